@@ -1,0 +1,180 @@
+/*
+ * dl_linear.h -- C ABI of the GB300 (sm_103a) decode-linear library.
+ *
+ * The operation (one decode linear layer):
+ *
+ *     y[m][n] = bias[n] + sum_k x[m][k] * w(n, k),   0 <= m < M <= 16
+ *
+ * with bf16 activations x[M][K], weights stored [N][K] (K contiguous), fp32
+ * accumulation and bf16 output rounded once, to nearest even.  This is the
+ * tall-skinny decode GEMV/GEMM of "Developing a custom Qwen2.5 72B inference
+ * engine from scratch" (§6.1 "Decode GEMV: already near the roofline": a
+ * memory-bound matrix times a token vector, measured by the fraction of peak
+ * HBM bandwidth it reaches; §2: every decoded token streams every weight once)
+ * and of "9% faster GLM-5.3-Flash prefill with GPU-to-GPU IPC" (section
+ * "TileLang: twice as fast, and no faster": a ~6-token verify step, 16-bit
+ * activations, weight-only FP8 with one scale per 128x128 block, the long K
+ * dimension split across blocks so that the whole chip streams weights).
+ *
+ * w(n, k) is either the bf16 weight W[n][k], or, for weight-only FP8,
+ * e4m3(Wq[n][k]) * scales[n / 128][k / 128]: the OCP E4M3FN code decoded
+ * exactly and multiplied by the fp32 scale of its 128x128 block (the TileLang
+ * loop's "B_h[i,k] = B_s[i,k] * S[nb, (kb*BK + k) // 128]").  Activations are
+ * never quantised (weight-only FP8; same engine page, §6.2).
+ *
+ * Conventions for every entry point below:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *    owned by the caller.  The library keeps no reference after a call
+ *    returns and allocates no device memory on any call path.
+ *  - Every tensor is dense and row-major exactly as described; there are no
+ *    stride arguments.
+ *  - Calls are asynchronous: work is enqueued on `stream` (a cudaStream_t
+ *    passed as void*; NULL = the legacy default stream) and the host is never
+ *    synchronised.  Results are valid once the stream has reached the call.
+ *  - All arguments are validated BEFORE anything is enqueued.  On a non-OK
+ *    status nothing was launched and nothing was written; dl_last_error()
+ *    returns a message for the calling thread.  No C++ exception crosses the
+ *    ABI.
+ *  - Shapes: 1 <= M <= 16; 1 <= N, K < 2^31; BF16 needs K % 8 == 0 and FP8
+ *    needs K % 128 == 0 (else DL_ERR_UNSUPPORTED_SHAPE).  x and W/Wq must be
+ *    16-byte aligned (DL_ERR_MISALIGNED); bias/y 2-byte, y_f32/scales 4-byte.
+ *  - Workspace: a device buffer of at least dl_workspace_bytes(...) bytes,
+ *    ZERO-FILLED ONCE before its first use.  Each call leaves it ready for the
+ *    next (its arrival counters return to zero), so it never needs clearing
+ *    again unless a call reported a device-side error.  Two calls that may run
+ *    at the same time (different streams) must not share a workspace.
+ *  - Results are deterministic: the same inputs, shape, device (SM count) and
+ *    overrides give bitwise identical outputs on every call.
+ */
+#ifndef DL_LINEAR_H
+#define DL_LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DL_VERSION 1
+
+typedef enum dl_status {
+    DL_OK = 0,
+    DL_ERR_INVALID_ARG = 1,        /* NULL pointer, bad enum, negative size      */
+    DL_ERR_UNSUPPORTED_SHAPE = 2,  /* M outside [1,16], K not a multiple of 8/128 */
+    DL_ERR_MISALIGNED = 3,         /* a pointer breaks its alignment rule         */
+    DL_ERR_WORKSPACE = 4,          /* workspace NULL or smaller than required     */
+    DL_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed           */
+    DL_ERR_DEVICE = 6              /* a kernel reported an error (dl_device_status) */
+} dl_status;
+
+/* Weight formats. */
+typedef enum dl_dtype {
+    DL_BF16 = 0,       /* W: bf16 [N][K]                                       */
+    DL_FP8_B128 = 1    /* Wq: e4m3 codes [N][K] + fp32 scales [ceil(N/128)][K/128] */
+} dl_dtype;
+
+/* Kernel families (for dl_set_override; DL_KERNEL_AUTO picks by dtype and M). */
+typedef enum dl_kernel {
+    DL_KERNEL_AUTO = 0,
+    DL_KERNEL_SIMT = 1,   /* CUDA-core FMA, one weight row per lane           */
+    DL_KERNEL_MMA = 2     /* warp-level bf16 tensor-core MMA (mma.sync)        */
+} dl_kernel;
+
+/*
+ * Bytes of workspace one call with this shape needs on the current device
+ * (it depends on the SM count and on any override set).  Returns 0 for an
+ * invalid shape or dtype.  Never launches anything.
+ */
+size_t dl_workspace_bytes(int M, int N, int K, int dtype);
+
+/*
+ * y = x . W^T (+ bias), bf16 weights.
+ *   x      bf16 [M][K], 16-byte aligned (K % 8 == 0 keeps every row aligned)
+ *   W      bf16 [N][K], 16-byte aligned
+ *   bias   bf16 [N] or NULL; added once in fp32 after the full K sum
+ *   y      bf16 [M][N]; written (round to nearest even, once)
+ *   y_f32  fp32 [M][N] or NULL; receives the value before rounding, so that
+ *          y == RNE_bf16(y_f32) bit for bit (a test/debug output)
+ *   workspace, ws_bytes: see the conventions above
+ *   stream cudaStream_t
+ */
+dl_status dl_linear_bf16(const void* x, const void* W, const void* bias, void* y,
+                         float* y_f32, int M, int N, int K, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/*
+ * y = x . dequant(Wq)^T (+ bias), weight-only FP8 with 128x128 block scales.
+ *   Wq     e4m3 (E4M3FN) codes [N][K] as bytes, 16-byte aligned, K % 128 == 0
+ *   scales fp32 [ceil(N/128)][K/128] row-major: scales[n/128][k/128]
+ *   other arguments as for dl_linear_bf16.
+ * Each e4m3 code is decoded exactly (NaN codes 0x7F/0xFF decode to NaN); the
+ * block scale multiplies the fp32 partial sum of each 128-wide K block, which
+ * is algebraically the same as scaling every weight.
+ */
+dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* scales,
+                                 const void* bias, void* y, float* y_f32, int M, int N,
+                                 int K, void* workspace, size_t ws_bytes, void* stream);
+
+/* One layer of a decode weight stream (see dl_decode_stream). */
+typedef struct dl_layer {
+    int dtype;             /* dl_dtype                                    */
+    int M, N, K;
+    const void* x;         /* bf16 [M][K]                                 */
+    const void* W;         /* bf16 [N][K] or e4m3 codes [N][K]            */
+    const float* scales;   /* FP8 only: fp32 [ceil(N/128)][K/128]; else NULL */
+    const void* bias;      /* bf16 [N] or NULL                            */
+    void* y;               /* bf16 [M][N]                                 */
+} dl_layer;
+
+/*
+ * Run layers[0..n_layers) back to back on one stream, in order, with no host
+ * synchronisation between them -- the whole weight stream of a decode step
+ * (e.g. 80 x {QKV, O, gate_up, down} + lm_head).  A layer may read the y of
+ * an earlier layer as its x.  All layers are validated before anything is
+ * enqueued.  ws_bytes must cover the largest layer.
+ * use_graph = 1: the sequence is captured once into a CUDA graph, cached
+ * under the exact contents of `layers` (pointers, shapes) + workspace, and
+ * replayed on later calls with the same list, removing per-launch host cost
+ * (a decode step replayed on the GPU with no host involvement; engine page §5).
+ * The first call with a new list captures on `stream`, which therefore must
+ * not itself be capturing.  dl_graph_cache_clear() drops cached graphs.
+ */
+dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace,
+                           size_t ws_bytes, void* stream, int use_graph);
+
+/* Destroy every cached graph (host call; synchronises nothing). */
+void dl_graph_cache_clear(void);
+
+/*
+ * Process-wide tuning overrides, for tests and tuning; 0 = automatic.
+ *   kernel       dl_kernel family to force
+ *   ctas_per_sm  resident CTAs per SM the grid is sized for (1 or 2)
+ *   max_ctas     upper bound on the grid (forces fewer K splits; 1 = one CTA)
+ * Changing an override changes dl_workspace_bytes and may change the last
+ * bits of results (a different split of K); any setting is correct.
+ * Not thread-safe against concurrent launches.
+ */
+dl_status dl_set_override(int kernel, int ctas_per_sm, int max_ctas);
+
+/*
+ * Read and clear the device error word of the current device: bit 0 = a
+ * consumer gave up waiting for a weight tile, bit 1 = the loader gave up
+ * waiting for a free stage, bit 2 = the final wait for copies in flight gave
+ * up.  Every device wait is bounded (about 2 s); a kernel that gives up sets a
+ * bit and returns instead of hanging.  SYNCHRONISES the device.  *flags may
+ * be NULL.  Returns DL_ERR_DEVICE if any bit was set.
+ */
+dl_status dl_device_status(unsigned int* flags);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* dl_last_error(void);
+
+/* DL_VERSION of the loaded library. */
+int dl_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* DL_LINEAR_H */

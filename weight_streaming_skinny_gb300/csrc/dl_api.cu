@@ -1,0 +1,454 @@
+// C-ABI host side of the decode-linear library: argument validation, the work
+// plan (grid, split of K, pipeline depth, workspace layout), TMA descriptor
+// encoding, launches, the layer-list stream with optional CUDA-graph replay,
+// and error reporting.  Nothing here allocates device memory or synchronises
+// the host, except dl_device_status (documented as synchronising).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/dl_linear.h"
+#include "dl_kernel.cuh"
+#include "dl_launch.h"
+
+// Device error word: bounded waits in the kernels OR their bit in here.
+__device__ unsigned int g_dl_device_error = 0;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+dl_status fail(dl_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+dl_status ok() {
+    g_err[0] = '\0';
+    return DL_OK;
+}
+
+std::atomic<int> g_kernel_override{0};
+std::atomic<int> g_cps_override{0};
+std::atomic<int> g_max_ctas_override{0};
+
+constexpr int kMaxStages = 16;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;
+    int smem_per_sm = 0;
+    unsigned* err_word = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+dl_status device_info(DeviceInfo& out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(DL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(DL_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+            return fail(DL_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_dl_device_error)) != cudaSuccess)
+            return fail(DL_ERR_CUDA, "cudaGetSymbolAddress(device error word): %s", cudaGetErrorString(e));
+        d.err_word = static_cast<unsigned*>(p);
+        d.ready = true;
+    }
+    out = d;
+    return DL_OK;
+}
+
+// The work plan of one call: kernel family, staged token rows, tiles, grid
+// and the split of the units among CTAs, pipeline depth, workspace layout.
+struct Plan {
+    int dtype, family, mt, mtb;
+    int KB, n_tiles;
+    long long units;
+    int grid;
+    long long q;
+    int r;
+    int stages;
+    size_t smem;
+    size_t tickets_off, partials_off, ws_bytes;
+};
+
+int auto_family(int dtype, int M) {
+    if (dtype == DL_BF16) return M <= 2 ? dl::kSIMT : dl::kMMA;
+    return M <= 1 ? dl::kSIMT : dl::kMMA;
+}
+
+int pow2_at_least(int M) {
+    int t = 1;
+    while (t < M) t <<= 1;
+    return t;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+dl_status check_shape(int dtype, int M, int N, int K) {
+    if (dtype != DL_BF16 && dtype != DL_FP8_B128)
+        return fail(DL_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (M < 1 || M > 16)
+        return fail(DL_ERR_UNSUPPORTED_SHAPE, "M=%d outside [1,16] (decode-only skinny GEMM)", M);
+    if (N < 1 || K < 1) return fail(DL_ERR_UNSUPPORTED_SHAPE, "N=%d and K=%d must be >= 1", N, K);
+    if (dtype == DL_BF16 && K % 8 != 0)
+        return fail(DL_ERR_UNSUPPORTED_SHAPE, "bf16 weights need K %% 8 == 0 (K=%d)", K);
+    if (dtype == DL_FP8_B128 && K % 128 != 0)
+        return fail(DL_ERR_UNSUPPORTED_SHAPE, "FP8 block-128 weights need K %% 128 == 0 (K=%d)", K);
+    return DL_OK;
+}
+
+dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& pl) {
+    pl.dtype = dtype;
+    const int ko = g_kernel_override.load();
+    pl.family = ko ? ko : auto_family(dtype, M);
+    if (pl.family != dl::kSIMT && pl.family != dl::kMMA)
+        return fail(DL_ERR_INVALID_ARG, "kernel override %d unknown", pl.family);
+    pl.mt = pl.family == dl::kMMA ? (M <= 8 ? 8 : 16) : pow2_at_least(M);
+    pl.mtb = dl::host_x_rows(pl.mt);
+    pl.KB = (K + dl::kBK - 1) / dl::kBK;
+    pl.n_tiles = (N + dl::kBN - 1) / dl::kBN;
+    pl.units = (long long)pl.n_tiles * pl.KB;
+    const int cps_o = g_cps_override.load();
+    const int cps = cps_o > 0 ? cps_o : 1;
+    long long grid = (long long)di.sm_count * cps;
+    const int mc = g_max_ctas_override.load();
+    if (mc > 0 && grid > mc) grid = mc;
+    if (grid > pl.units) grid = pl.units;
+    if (grid < 1) grid = 1;
+    pl.grid = (int)grid;
+    pl.q = pl.units / pl.grid;
+    pl.r = (int)(pl.units % pl.grid);
+    // Pipeline depth: as many stages as the shared memory of one CTA (out of
+    // `cps` resident per SM) holds.
+    int budget = di.smem_optin;
+    const int per_sm = di.smem_per_sm / cps - 1024;
+    if (per_sm < budget) budget = per_sm;
+    const int stage = dl::host_stage_bytes(dtype == DL_BF16 ? dl::kBF16 : dl::kFP8, pl.mt);
+    int stages = kMaxStages;
+    while (stages > 2 && (size_t)stages * stage + dl::host_fixed_smem_bytes(pl.mt, stages) + 1024 >
+                             (size_t)budget)
+        --stages;
+    if ((size_t)stages * stage + dl::host_fixed_smem_bytes(pl.mt, stages) + 1024 > (size_t)budget)
+        return fail(DL_ERR_UNSUPPORTED_SHAPE, "not enough shared memory for two pipeline stages");
+    pl.stages = stages;
+    pl.smem = (size_t)stages * stage + dl::host_fixed_smem_bytes(pl.mt, stages) + 1024;
+    pl.tickets_off = 0;
+    pl.partials_off = align_up((size_t)pl.n_tiles * sizeof(int), 256);
+    pl.ws_bytes = pl.partials_off + (size_t)pl.grid * 2 * pl.mtb * dl::kBN * sizeof(float);
+    return DL_OK;
+}
+
+// ----------------------------------------------------------------- TMA descriptors
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+dl_status get_encode(EncodeTiledFn& fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!g_encode) return fail(DL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    fn = g_encode;
+    return DL_OK;
+}
+
+dl_status encode_maps(const Plan& pl, int M, int N, int K, const void* x, const void* W,
+                      CUtensorMap& tw, CUtensorMap& tx) {
+    EncodeTiledFn enc;
+    dl_status s = get_encode(enc);
+    if (s != DL_OK) return s;
+    const cuuint32_t ones[3] = {1, 1, 1};
+    CUresult r;
+    if (pl.dtype == DL_BF16) {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)dl::kBN};
+        r = enc(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims, strides, box,
+                ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K};
+        const cuuint32_t box[2] = {128, (cuuint32_t)dl::kBN};
+        r = enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box,
+                ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return fail(DL_ERR_CUDA, "weight tensor map: CUresult %d", (int)r);
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)pl.mtb};
+        r = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
+                ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return fail(DL_ERR_CUDA, "activation tensor map: CUresult %d", (int)r);
+    return DL_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Host-only checks of one layer (no CUDA call).
+dl_status validate(int dtype, int M, int N, int K, const void* x, const void* W,
+                   const float* scales, const void* bias, const void* y, const float* y_f32) {
+    dl_status s = check_shape(dtype, M, N, K);
+    if (s != DL_OK) return s;
+    if (!x || !W || !y) return fail(DL_ERR_INVALID_ARG, "x, W and y must be non-NULL");
+    if (dtype == DL_FP8_B128 && !scales)
+        return fail(DL_ERR_INVALID_ARG, "FP8 block-128 weights need scales");
+    if (!aligned(x, 16) || !aligned(W, 16))
+        return fail(DL_ERR_MISALIGNED, "x and W must be 16-byte aligned");
+    if (!aligned(y, 2) || (bias && !aligned(bias, 2)))
+        return fail(DL_ERR_MISALIGNED, "y and bias must be 2-byte aligned");
+    if ((y_f32 && !aligned(y_f32, 4)) || (scales && !aligned(scales, 4)))
+        return fail(DL_ERR_MISALIGNED, "y_f32 and scales must be 4-byte aligned");
+    return DL_OK;
+}
+
+dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void* W,
+                       const float* scales, const void* bias, void* y, float* y_f32,
+                       void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di) {
+    Plan pl;
+    dl_status s = make_plan(dtype, M, N, K, di, pl);
+    if (s != DL_OK) return s;
+    if (!ws) return fail(DL_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(DL_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    if (ws_bytes < pl.ws_bytes)
+        return fail(DL_ERR_WORKSPACE, "workspace has %zu bytes, this call needs %zu", ws_bytes,
+                    pl.ws_bytes);
+    CUtensorMap tw, tx;
+    if ((s = encode_maps(pl, M, N, K, x, W, tw, tx)) != DL_OK) return s;
+    dl::LinearParams p;
+    p.bias = static_cast<const uint16_t*>(bias);
+    p.y = static_cast<uint16_t*>(y);
+    p.y_f32 = y_f32;
+    p.scales = scales;
+    p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.tickets_off);
+    p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.partials_off);
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.KB = pl.KB;
+    p.n_tiles = pl.n_tiles;
+    p.q = pl.q;
+    p.r = pl.r;
+    p.stages = pl.stages;
+    p.err = di.err_word;
+    cudaError_t e = dtype == DL_BF16
+        ? dl::launch_linear_bf16(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true)
+        : dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
+    if (e != cudaSuccess) return fail(DL_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    return DL_OK;
+}
+
+// Raise the shared-memory ceiling of the kernel instance a layer will use
+// (host-side, once per device) so that a later stream capture contains only
+// launches.
+dl_status prepare_layer(int dtype, int M, int N, int K, const DeviceInfo& di) {
+    Plan pl;
+    dl_status s = make_plan(dtype, M, N, K, di, pl);
+    if (s != DL_OK) return s;
+    CUtensorMap tw, tx;
+    dl::LinearParams p;
+    cudaError_t e = dtype == DL_BF16
+        ? dl::launch_linear_bf16(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, nullptr, false)
+        : dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, nullptr, false);
+    if (e != cudaSuccess) return fail(DL_ERR_CUDA, "kernel attribute: %s", cudaGetErrorString(e));
+    return DL_OK;
+}
+
+// ----------------------------------------------------------------- graph cache
+
+std::mutex g_graph_mu;
+std::map<std::string, cudaGraphExec_t> g_graphs;
+
+}  // namespace
+
+extern "C" {
+
+int dl_version(void) { return DL_VERSION; }
+
+const char* dl_last_error(void) { return g_err; }
+
+dl_status dl_set_override(int kernel, int ctas_per_sm, int max_ctas) {
+    if (kernel < 0 || kernel > 2) return fail(DL_ERR_INVALID_ARG, "kernel override %d unknown", kernel);
+    if (ctas_per_sm < 0 || ctas_per_sm > 2)
+        return fail(DL_ERR_INVALID_ARG, "ctas_per_sm must be 0, 1 or 2");
+    if (max_ctas < 0) return fail(DL_ERR_INVALID_ARG, "max_ctas must be >= 0");
+    g_kernel_override.store(kernel);
+    g_cps_override.store(ctas_per_sm);
+    g_max_ctas_override.store(max_ctas);
+    return ok();
+}
+
+size_t dl_workspace_bytes(int M, int N, int K, int dtype) {
+    if (check_shape(dtype, M, N, K) != DL_OK) return 0;
+    DeviceInfo di;
+    if (device_info(di) != DL_OK) return 0;
+    Plan pl;
+    if (make_plan(dtype, M, N, K, di, pl) != DL_OK) return 0;
+    return pl.ws_bytes;
+}
+
+dl_status dl_linear_bf16(const void* x, const void* W, const void* bias, void* y, float* y_f32,
+                         int M, int N, int K, void* workspace, size_t ws_bytes, void* stream) {
+    dl_status s = validate(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32);
+    if (s != DL_OK) return s;
+    if (!workspace) return fail(DL_ERR_WORKSPACE, "workspace is NULL");
+    DeviceInfo di;
+    if ((s = device_info(di)) != DL_OK) return s;
+    s = launch_layer(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32, workspace, ws_bytes,
+                     static_cast<cudaStream_t>(stream), di);
+    return s == DL_OK ? ok() : s;
+}
+
+dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* scales,
+                                 const void* bias, void* y, float* y_f32, int M, int N, int K,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+    dl_status s = validate(DL_FP8_B128, M, N, K, x, Wq, scales, bias, y, y_f32);
+    if (s != DL_OK) return s;
+    if (!workspace) return fail(DL_ERR_WORKSPACE, "workspace is NULL");
+    DeviceInfo di;
+    if ((s = device_info(di)) != DL_OK) return s;
+    s = launch_layer(DL_FP8_B128, M, N, K, x, Wq, scales, bias, y, y_f32, workspace, ws_bytes,
+                     static_cast<cudaStream_t>(stream), di);
+    return s == DL_OK ? ok() : s;
+}
+
+dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace, size_t ws_bytes,
+                           void* stream, int use_graph) {
+    if (n_layers < 0 || (n_layers > 0 && !layers))
+        return fail(DL_ERR_INVALID_ARG, "layers must be non-NULL when n_layers > 0");
+    if (use_graph != 0 && use_graph != 1) return fail(DL_ERR_INVALID_ARG, "use_graph must be 0 or 1");
+    for (int i = 0; i < n_layers; ++i) {
+        const dl_layer& L = layers[i];
+        dl_status s = validate(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr);
+        if (s != DL_OK) {
+            std::string m = g_err;
+            return fail(s, "layer %d: %s", i, m.c_str());
+        }
+    }
+    if (n_layers == 0) return ok();
+    if (!workspace) return fail(DL_ERR_WORKSPACE, "workspace is NULL");
+    DeviceInfo di;
+    dl_status s = device_info(di);
+    if (s != DL_OK) return s;
+    // Check every layer's plan against the workspace before enqueuing anything.
+    for (int i = 0; i < n_layers; ++i) {
+        const dl_layer& L = layers[i];
+        Plan pl;
+        if ((s = make_plan(L.dtype, L.M, L.N, L.K, di, pl)) != DL_OK) return s;
+        if (ws_bytes < pl.ws_bytes)
+            return fail(DL_ERR_WORKSPACE, "layer %d needs %zu workspace bytes, have %zu", i,
+                        pl.ws_bytes, ws_bytes);
+        if ((s = prepare_layer(L.dtype, L.M, L.N, L.K, di)) != DL_OK) return s;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto enqueue_all = [&]() -> dl_status {
+        for (int i = 0; i < n_layers; ++i) {
+            const dl_layer& L = layers[i];
+            dl_status r = launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y,
+                                       nullptr, workspace, ws_bytes, st, di);
+            if (r != DL_OK) {
+                std::string m = g_err;
+                return fail(r, "layer %d: %s", i, m.c_str());
+            }
+        }
+        return DL_OK;
+    };
+    if (!use_graph) {
+        s = enqueue_all();
+        return s == DL_OK ? ok() : s;
+    }
+    if (st == nullptr)
+        return fail(DL_ERR_INVALID_ARG, "graph replay needs a non-default stream");
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::string key(reinterpret_cast<const char*>(layers), sizeof(dl_layer) * (size_t)n_layers);
+    const long long extra[6] = {(long long)(uintptr_t)workspace, (long long)ws_bytes, dev,
+                                g_kernel_override.load(), g_cps_override.load(),
+                                g_max_ctas_override.load()};
+    key.append(reinterpret_cast<const char*>(extra), sizeof extra);
+    cudaGraphExec_t exec = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_graph_mu);
+        auto it = g_graphs.find(key);
+        if (it != g_graphs.end()) exec = it->second;
+    }
+    cudaError_t e;
+    if (!exec) {
+        if ((e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal)) != cudaSuccess)
+            return fail(DL_ERR_CUDA, "cudaStreamBeginCapture: %s", cudaGetErrorString(e));
+        dl_status r = enqueue_all();
+        cudaGraph_t graph = nullptr;
+        e = cudaStreamEndCapture(st, &graph);
+        if (r != DL_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return r;
+        }
+        if (e != cudaSuccess) return fail(DL_ERR_CUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(e));
+        e = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return fail(DL_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
+        std::lock_guard<std::mutex> lk(g_graph_mu);
+        g_graphs[key] = exec;
+    }
+    if ((e = cudaGraphLaunch(exec, st)) != cudaSuccess)
+        return fail(DL_ERR_CUDA, "cudaGraphLaunch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+void dl_graph_cache_clear(void) {
+    std::lock_guard<std::mutex> lk(g_graph_mu);
+    for (auto& kv : g_graphs) cudaGraphExecDestroy(kv.second);
+    g_graphs.clear();
+}
+
+dl_status dl_device_status(unsigned int* flags) {
+    unsigned v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(DL_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    if ((e = cudaMemcpyFromSymbol(&v, g_dl_device_error, sizeof v)) != cudaSuccess)
+        return fail(DL_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+    const unsigned zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_dl_device_error, &zero, sizeof zero)) != cudaSuccess)
+        return fail(DL_ERR_CUDA, "clearing the device error word: %s", cudaGetErrorString(e));
+    if (flags) *flags = v;
+    if (v) return fail(DL_ERR_DEVICE, "device error word 0x%x (a bounded wait gave up)", v);
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Instantiation helper shared by the per-dtype kernel translation units.
+#pragma once
+
+#include <atomic>
+
+#include "dl_kernel.cuh"
+#include "dl_launch.h"
+
+namespace dl {
+
+// Raise the instance's dynamic shared-memory ceiling to `smem` on the current
+// device, once per device (a host-side function attribute, never enqueued).
+template <int DT, int FAM, int MT>
+cudaError_t prepare_instance(size_t smem) {
+    static std::atomic<int> set_bytes[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (set_bytes[dev].load() >= (int)smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(linear_kernel<DT, FAM, MT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) set_bytes[dev].store((int)smem);
+    return e;
+}
+
+template <int DT, int FAM, int MT>
+cudaError_t launch_instance(const CUtensorMap& tw, const CUtensorMap& tx, const LinearParams& p,
+                            int grid, size_t smem, cudaStream_t stream, bool launch) {
+    cudaError_t e = prepare_instance<DT, FAM, MT>(smem);
+    if (e != cudaSuccess || !launch) return e;
+    linear_kernel<DT, FAM, MT><<<grid, kThreads, smem, stream>>>(tw, tx, p);
+    return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_family(int family, int mt, const CUtensorMap& tw, const CUtensorMap& tx,
+                          const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
+                          bool launch) {
+    if (family == kMMA) {
+        if (mt == 8) return launch_instance<DT, kMMA, 8>(tw, tx, p, grid, smem, stream, launch);
+        if (mt == 16) return launch_instance<DT, kMMA, 16>(tw, tx, p, grid, smem, stream, launch);
+        return cudaErrorInvalidValue;
+    }
+    switch (mt) {
+        case 1: return launch_instance<DT, kSIMT, 1>(tw, tx, p, grid, smem, stream, launch);
+        case 2: return launch_instance<DT, kSIMT, 2>(tw, tx, p, grid, smem, stream, launch);
+        case 4: return launch_instance<DT, kSIMT, 4>(tw, tx, p, grid, smem, stream, launch);
+        case 8: return launch_instance<DT, kSIMT, 8>(tw, tx, p, grid, smem, stream, launch);
+        case 16: return launch_instance<DT, kSIMT, 16>(tw, tx, p, grid, smem, stream, launch);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dl
