@@ -9,9 +9,14 @@ byte is ever an L2 hit between steps.  The metric is achieved HBM bandwidth:
 algorithmic bytes (weights + scales + x + y + bias) / device time, reported
 absolutely and as a fraction of the measured HBM copy bandwidth.
 
-`--workload fp8_m6` times the same four shapes with weight-only FP8
-block-128 weights at M=6; `--workload decode_stream` times the whole-model
-weight stream (80 FP8 layers + bf16 lm_head, M=1) as ms/token.
+A step runs through the layer-list entry point (dl_decode_stream), replayed as
+a cached CUDA graph (`--mode graph`, default); `--mode calls` issues one API
+call per layer.  Per-layer figures come from separate single calls with
+events around each kernel.
+
+`--workload qwen72b_layer_fp8_m6` times the same four shapes with weight-only
+FP8 block-128 weights at M=6; `--workload qwen72b_model_fp8_m1` times the
+whole-model weight stream (80 FP8 layers + bf16 lm_head, M=1) as ms/token.
 
 `--impl reference` times the CPU oracle (the only other arm: no reference
 implementation exists) on a bounded sample of the same workload.
@@ -138,23 +143,45 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workloads
 
+WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8_m1"]
+
+
 def layer_specs(workload: str):
+    """[(dtype, M, N, K, bias, name)], config id."""
     from weight_streaming_skinny_gb300 import inputs
     shapes = inputs.QWEN72B_SHAPES
     if workload == "qwen72b_layer_bf16_m1":
         return [(inputs.DTYPE_BF16, 1, *shapes[n][:2], shapes[n][2], n) for n in shapes], 1
     if workload == "qwen72b_layer_fp8_m6":
         return [(inputs.DTYPE_FP8_B128, 6, *shapes[n][:2], shapes[n][2], n) for n in shapes], 2
+    if workload == "qwen72b_model_fp8_m1":
+        specs = []
+        for layer in range(inputs.QWEN72B_LAYERS):
+            for n in shapes:
+                specs.append((inputs.DTYPE_FP8_B128, 1, *shapes[n][:2], shapes[n][2], f"{n}.{layer}"))
+        N, K, b = inputs.QWEN72B_LM_HEAD
+        specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head"))
+        return specs, 4
     raise ValueError(workload)
 
 
 def build_layers(workload, dev):
+    """Seeded layers on `dev`.  In the whole-model stream, a layer reads the
+    previous layer's output when the shapes chain (down -> next QKV, O ->
+    gate_up); attention and the MLP activation are not part of this path, so O
+    and down read fixed activation buffers."""
+    import torch
     from weight_streaming_skinny_gb300 import inputs
     specs, cfg = layer_specs(workload)
     out = []
     for i, (dt, M, N, K, bias, name) in enumerate(specs):
         L = inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg, layer_idx=i, device=dev)
         out.append((name, L))
+    if workload == "qwen72b_model_fp8_m1":
+        for i in range(1, len(out)):
+            prev, cur = out[i - 1][1], out[i][1]
+            if prev.N == cur.K and prev.M == cur.M and out[i][0].split(".")[0] in ("qkv", "gate_up", "lm_head"):
+                cur.x = None          # chained: filled with the previous layer's y below
     return out
 
 
@@ -174,32 +201,37 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dl.load()
+    dl.set_override({"auto": 0, "simt": 1, "mma": 2}[args.kernel], 0, 0)
     workload = args.workload
     layers = build_layers(workload, dev)
     ys = [torch.empty((L.M, L.N), dtype=torch.bfloat16, device=dev) for _, L in layers]
+    for j in range(1, len(layers)):
+        if layers[j][1].x is None:
+            layers[j][1].x = ys[j - 1]
     ws = dl.Workspace.for_shapes(
         [(L.M, L.N, L.K, dl.BF16 if L.dtype == "bf16" else dl.FP8_B128) for _, L in layers], dev)
     stream = torch.cuda.Stream(dev)
     nbytes = [L.algorithmic_bytes for _, L in layers]
     step_bytes = sum(nbytes)
+    dl_layers = [dl.Layer(dl.BF16 if L.dtype == "bf16" else dl.FP8_B128, L.x, L.w, ys[j],
+                          L.scales, L.bias) for j, (_, L) in enumerate(layers)]
+    use_graph = args.mode == "graph"
     torch.cuda.synchronize(dev)
 
-    def step(evs=None):
-        for j, (_, L) in enumerate(layers):
-            if evs is not None:
-                evs[j].record(stream)
-            launch(dl, L, ys[j], ws, stream)
-        if evs is not None:
-            evs[len(layers)].record(stream)
+    def step():
+        if args.mode == "calls":
+            for j, (_, L) in enumerate(layers):
+                launch(dl, L, ys[j], ws, stream)
+        else:
+            dl.decode_stream(dl_layers, ws, use_graph=use_graph, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
     stream.synchronize()
 
-    # ---- timed region: exactly K steps, per-kernel events on the launching stream
+    # ---- timed region: exactly K steps, CUDA events on the launching stream
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(layers) + 1)] for _ in range(K)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -211,7 +243,7 @@ def run_ours(args, rank, world, dist):
     with torch.cuda.stream(stream):
         t0.record(stream)
         for k in range(K):
-            step(evs[k])
+            step()
         t1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize(dev)
@@ -222,14 +254,12 @@ def run_ours(args, rank, world, dist):
     deadline = time.time() + 3.0
     while len(sampler.lines) < 5 and time.time() < deadline:
         with torch.cuda.stream(stream):
-            for _ in range(20):
+            for _ in range(10):
                 step()
         stream.synchronize()
-        extra_steps += 20
+        extra_steps += 10
     sampler.stop()
     total_ms = t0.elapsed_time(t1)
-    per_layer_ms = [sum(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(K)) / K
-                    for j in range(len(layers))]
     if dist is not None:
         import torch.distributed as tdist
         t = torch.tensor([total_ms], dtype=torch.float64)
@@ -238,22 +268,46 @@ def run_ours(args, rank, world, dist):
     ms_per_step = total_ms / K
     value = step_bytes * world * K / (total_ms * 1e-3) / 1e9
 
+    # ---- per-layer breakdown (single calls, events around each kernel; untimed)
+    per_layer = {}
+    if len(layers) <= 8:
+        R = 20
+        with torch.cuda.stream(stream):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(layers) + 1)]
+                   for _ in range(R)]
+            for r in range(R):
+                for j, (_, L) in enumerate(layers):
+                    evs[r][j].record(stream)
+                    launch(dl, L, ys[j], ws, stream)
+                evs[r][len(layers)].record(stream)
+        stream.synchronize()
+        peak0, _ = measured_peak()
+        for j, (name, L) in enumerate(layers):
+            ms = sum(evs[r][j].elapsed_time(evs[r][j + 1]) for r in range(R)) / R
+            b = nbytes[j]
+            per_layer[name] = {"us": round(ms * 1e3, 3), "bytes": b,
+                               "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                               "frac_measured": round(b / (ms * 1e-3) / 1e9 / peak0, 4)}
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.skip_e2e:
+        chained_in = [j > 0 and layers[j][1].x is ys[j - 1] for j in range(len(layers))]
+        chained_out = [j + 1 < len(layers) and chained_in[j + 1] for j in range(len(layers))]
         hx = [L.x.cpu().pin_memory() for _, L in layers]
         hy = [torch.empty((L.M, L.N), dtype=torch.bfloat16).pin_memory() for _, L in layers]
-        dx = [torch.empty_like(L.x) for _, L in layers]
-        h2d = sum(x.numel() * 2 for x in hx)
-        d2h = sum(y.numel() * 2 for y in hy)
+        h2d = sum(x.numel() * 2 for j, x in enumerate(hx) if not chained_in[j])
+        d2h = sum(y.numel() * 2 for j, y in enumerate(hy) if not chained_out[j])
         E = max(3, min(K, 50))
 
         def e2e_step():
             for j, (_, L) in enumerate(layers):
-                dx[j].copy_(hx[j], non_blocking=True)
-                Lj = inputs.LayerInputs(L.dtype, L.M, L.N, L.K, dx[j], L.w, L.scales, L.bias)
-                launch(dl, Lj, ys[j], ws, stream)
-                hy[j].copy_(ys[j], non_blocking=True)
+                if j == 0 or layers[j][1].x is not ys[j - 1]:
+                    L.x.copy_(hx[j], non_blocking=True)
+            step()
+            for j in range(len(layers)):
+                if j == len(layers) - 1 or layers[j + 1][1].x is not ys[j]:
+                    hy[j].copy_(ys[j], non_blocking=True)
             stream.synchronize()
 
         with torch.cuda.stream(stream):
@@ -275,25 +329,24 @@ def run_ours(args, rank, world, dist):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "x copied host->device and y device->host every step; weights resident in HBM"}
 
-    # ---- roofline of the dominant kernel (all four layers run one kernel instance)
+    # ---- roofline of the dominant kernel: every launch of the step is the one
+    # decode-linear kernel, so its average launch duration is the step time
+    # divided by the launches per step (CUDA events on the launching stream).
     peak, peak_kind = measured_peak()
     kname = "linear_kernel"
-    k_bytes = sum(nbytes)
-    k_ms = sum(per_layer_ms)
-    achieved = k_bytes / (k_ms * 1e-3) / 1e9
+    avg_launch_ms = ms_per_step / len(layers)
+    achieved = (step_bytes / len(layers)) / (avg_launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": recorded_traffic(workload, kname),
-                "kernel": kname, "bytes_per_launch_avg": int(k_bytes / len(layers)),
-                "avg_launch_us": round(k_ms / len(layers) * 1e3, 3)}
-    per_layer = {name: {"us": round(ms * 1e3, 3), "bytes": b,
-                        "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
-                        "frac_measured": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
-                 for (name, _), ms, b in zip(layers, per_layer_ms, nbytes)}
+                "kernel": kname, "bytes_per_launch_avg": int(step_bytes / len(layers)),
+                "avg_launch_us": round(avg_launch_ms * 1e3, 3)}
     return {
         "value": round(value, 2), "ms_per_step": round(ms_per_step, 5), "e2e": e2e,
         "roofline": roofline, "per_layer": per_layer, "clocks": sampler.summary(),
+        "ms_per_token": round(ms_per_step, 4),
+        "ceiling_ms_at_measured_peak": round(step_bytes / (peak * 1e9) * 1e3, 4),
         "clock_window": f"timed region + {extra_steps} untimed steps of the same workload",
         "gpu_launches": len(layers) * K, "step_bytes": step_bytes,
     }, layers
@@ -337,8 +390,12 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen72b_layer_bf16_m1",
-                    choices=["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6"])
+    ap.add_argument("--workload", default="qwen72b_layer_bf16_m1", choices=WORKLOADS)
+    ap.add_argument("--mode", choices=["graph", "stream", "calls"], default="graph",
+                    help="graph: one dl_decode_stream CUDA-graph replay per step (default); "
+                         "stream: dl_decode_stream without a graph; calls: one API call per layer")
+    ap.add_argument("--kernel", choices=["auto", "simt", "mma"], default="auto",
+                    help="force a kernel family (default: the library's automatic choice)")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the end-to-end leg")
     ap.add_argument("--skip-cpu-baseline", action="store_true", help="omit the oracle timing leg")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
@@ -360,13 +417,28 @@ def main():
                           "bias": s[4]} for s in specs],
               "l2": "inputs larger than L2: every step streams all four weight matrices "
                     "(>= 0.88 GB) through a 129 MB L2",
-              "parallelism": f"replicas x{world}"}
+              "parallelism": f"replicas x{world}", "kernel_family": args.kernel,
+              "mode": args.mode}
+    if len(specs) > 8:
+        config["layers"] = {"count": len(specs), "decoder_layers": len(specs) // 4,
+                            "per_layer": [s[5].split(".")[0] for s in specs[:4]],
+                            "dtype": specs[0][0], "M": specs[0][1], "lm_head": "bf16 152064x8192"}
 
     if args.impl == "reference":
         if rank != 0:
             return
         import torch
-        layers = build_layers(args.workload, "cpu")
+        if args.workload == "qwen72b_model_fp8_m1":
+            # bounded sample: decoder layer 0 and the lm_head (not 72 GB of host weights)
+            from weight_streaming_skinny_gb300 import inputs
+            specs_all, cfg = layer_specs(args.workload)
+            layers = []
+            for i in (0, 1, 2, 3, len(specs_all) - 1):
+                dt, M, N, K, bias, name = specs_all[i]
+                layers.append((name, inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg,
+                                                       layer_idx=i, device="cpu")))
+        else:
+            layers = build_layers(args.workload, "cpu")
         sample_frac = 0.25
         for _ in range(args.warmup):
             cpu_oracle_gbs(layers, 0.0, sample_frac)
@@ -388,17 +460,22 @@ def main():
                 "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
-        del torch
         return
 
     res, layers = run_ours(args, rank, world, dist)
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
-        host_layers = [(n, L.to("cpu")) for n, L in layers]
+        if len(layers) > 8:
+            pick = [0, 1, 2, 3, len(layers) - 1]
+            host_layers = [(layers[i][0], layers[i][1].to("cpu")) for i in pick]
+            what = ("decoder layer 0 (QKV, O, gate_up, down) and the lm_head, all rows; GB/s "
+                    "applies to the whole 80-layer stream by extrapolation")
+        else:
+            host_layers = [(n, L.to("cpu")) for n, L in layers]
+            what = "the whole step (all rows of the four linears)"
         v, threads, passes, t = cpu_oracle_gbs(host_layers, args.cpu_budget_s, 1.0)
         cpu = {"value": round(v, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"the whole step (all rows of the four linears), {passes} pass(es), "
-                         f"{t:.1f} s of oracle time"}
+               "sample": f"{what}, {passes} pass(es), {t:.1f} s of oracle time"}
     if rank == 0:
         line = {"metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
@@ -407,6 +484,8 @@ def main():
                 "config": config, "roofline": res["roofline"], "cpu_baseline": cpu,
                 "e2e": res["e2e"], "clocks": res["clocks"], "clock_window": res["clock_window"],
                 "gpu_launches": res["gpu_launches"], "per_layer": res["per_layer"],
+                "ms_per_token": res["ms_per_token"],
+                "ceiling_ms_at_measured_peak": res["ceiling_ms_at_measured_peak"],
                 "step_bytes": res["step_bytes"], "kernel_hash": kernel_hash()}
         print(json.dumps(line), flush=True)
     if dist is not None:

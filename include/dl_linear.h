@@ -77,7 +77,8 @@ typedef enum dl_dtype {
 /* Kernel families (for dl_set_override; DL_KERNEL_AUTO picks by dtype and M). */
 typedef enum dl_kernel {
     DL_KERNEL_AUTO = 0,
-    DL_KERNEL_SIMT = 1,   /* CUDA-core FMA, one weight row per lane           */
+    DL_KERNEL_SIMT = 1,   /* CUDA-core FMA, one weight row per lane (FP8: M <= 2;
+                             larger M runs the MMA family)                    */
     DL_KERNEL_MMA = 2     /* warp-level bf16 tensor-core MMA (mma.sync)        */
 } dl_kernel;
 
@@ -149,8 +150,10 @@ void dl_graph_cache_clear(void);
 /*
  * Process-wide tuning overrides, for tests and tuning; 0 = automatic.
  *   kernel       dl_kernel family to force
- *   ctas_per_sm  resident CTAs per SM the grid is sized for (1 or 2)
- *   max_ctas     upper bound on the grid (forces fewer K splits; 1 = one CTA)
+ *   ctas_per_sm  resident CTAs per SM the persistent grid is sized for: 1
+ *                (one CTA with all of the SM's shared memory) or 2 (two, half
+ *                each); 0 = 1
+ *   max_ctas     upper bound on the grid (1 = a single CTA)
  * Changing an override changes dl_workspace_bytes and may change the last
  * bits of results (a different split of K); any setting is correct.
  * Not thread-safe against concurrent launches.

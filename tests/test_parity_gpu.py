@@ -243,9 +243,28 @@ def test_guard_bands_untouched(cuda_device, family):
         assert torch.all(ybuf[:G] == -7.0) and torch.all(ybuf[G + M * N:] == -7.0)
         assert torch.all(fbuf[:G] == -7.0) and torch.all(fbuf[G + M * N:] == -7.0)
         assert torch.all(wsbuf[need:] == 0xAB)
-        # the arrival tickets are back to zero after the call
-        n_tiles = (N + 127) // 128
-        assert torch.all(wsbuf[:4 * n_tiles] == 0)
+        # the whole workspace (tickets and partials) is back to zero after the call
+        assert torch.all(wsbuf[:need] == 0)
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+def test_one_workspace_serves_calls_of_any_shape(cuda_device, family):
+    """Calls with few tiles then many tiles share one workspace: every call leaves
+    it all-zero, so no call ever reads a stale arrival ticket."""
+    dl.set_override(family, 0, 0)
+    shapes = [(inputs.DTYPE_BF16, 1, 300, 8192), (inputs.DTYPE_FP8_B128, 6, 640, 8192),
+              (inputs.DTYPE_BF16, 2, 20000, 1024), (inputs.DTYPE_FP8_B128, 9, 30000, 1024),
+              (inputs.DTYPE_BF16, 16, 300, 8192), (inputs.DTYPE_BF16, 1, 40000, 512)]
+    need = max(dl.workspace_bytes(M, N, K, dl.BF16 if dt == inputs.DTYPE_BF16 else dl.FP8_B128)
+               for dt, M, N, K in shapes)
+    ws = dl.Workspace(need, cuda_device)
+    for i, (dt, M, N, K) in enumerate(shapes):
+        L = inputs.make_layer(dt, M, N, K, bias=(i % 2 == 0), config_id=46, layer_idx=i)
+        y, y32 = run_gpu(L.to(cuda_device), cuda_device, workspace=ws)
+        rows = sample_rows(N, count=64, seed=i)
+        ref, a = oracle_for(L, rows=rows)
+        assert_parity(y, y32, ref, a, rows=rows, what=f"shared workspace call {i}")
+        assert torch.all(ws.tensor == 0), f"workspace not all-zero after call {i}"
 
 
 def test_workspace_too_small_is_rejected_before_launch(cuda_device):
@@ -287,11 +306,14 @@ def test_decode_stream_matches_single_calls_and_oracle(cuda_device):
         else:
             dl.linear_fp8_block128(L.x, L.w, L.scales, L.bias, out=L.y, workspace=ws)
         singles.append(L.y.clone())
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()          # graph capture needs a non-default stream
     for use_graph in (False, True, True):
         for L in layers:
             L.y.fill_(0)
-        dl.decode_stream(layers, ws, use_graph=use_graph, stream=torch.cuda.current_stream())
         torch.cuda.synchronize()
+        dl.decode_stream(layers, ws, use_graph=use_graph, stream=st)
+        st.synchronize()
         for i, L in enumerate(layers):
             assert torch.equal(L.y, singles[i]), (use_graph, i)
     # oracle, one layer at a time on the GPU's own input bytes

@@ -147,6 +147,8 @@ class Workspace:
     def __init__(self, nbytes: int, device="cuda"):
         self.nbytes = max(int(nbytes), 256)
         self.tensor = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+        # the zeros must be in place before a kernel on any stream reads them
+        torch.cuda.synchronize(self.tensor.device)
 
     @classmethod
     def for_shapes(cls, shapes, device="cuda"):
@@ -157,6 +159,7 @@ class Workspace:
 
     def reset(self):
         self.tensor.zero_()
+        torch.cuda.synchronize(self.tensor.device)
 
     @property
     def ptr(self):

@@ -15,7 +15,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/dl_linear.h"
+#include "dl_linear.h"
 #include "dl_kernel.cuh"
 #include "dl_launch.h"
 
@@ -86,16 +86,19 @@ struct Plan {
     int KB, n_tiles;
     long long units;
     int grid;
-    long long q;
-    int r;
+    int n_segments;
+    int n_waves;
+    int wave_seg0[dl::kMaxWaves + 1];
+    long long wave_unit0[dl::kMaxWaves];
+    int wave_size[dl::kMaxWaves];
     int stages;
     size_t smem;
-    size_t tickets_off, partials_off, ws_bytes;
+    size_t counter_off, tickets_off, partials_off, ws_bytes;
 };
 
 int auto_family(int dtype, int M) {
     if (dtype == DL_BF16) return M <= 2 ? dl::kSIMT : dl::kMMA;
-    return M <= 1 ? dl::kSIMT : dl::kMMA;
+    return dl::kMMA;
 }
 
 int pow2_at_least(int M) {
@@ -125,38 +128,84 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     pl.family = ko ? ko : auto_family(dtype, M);
     if (pl.family != dl::kSIMT && pl.family != dl::kMMA)
         return fail(DL_ERR_INVALID_ARG, "kernel override %d unknown", pl.family);
+    // The CUDA-core family decodes FP8 for at most 2 tokens; beyond, the
+    // decode cost per code is the same and only the MMA amortises the FMAs.
+    if (pl.family == dl::kSIMT && dtype == DL_FP8_B128 && M > 2) pl.family = dl::kMMA;
     pl.mt = pl.family == dl::kMMA ? (M <= 8 ? 8 : 16) : pow2_at_least(M);
     pl.mtb = dl::host_x_rows(pl.mt);
     pl.KB = (K + dl::kBK - 1) / dl::kBK;
     pl.n_tiles = (N + dl::kBN - 1) / dl::kBN;
     pl.units = (long long)pl.n_tiles * pl.KB;
+    // Grid: persistent, `cps` CTAs per SM: by default one, with all of the
+    // SM's shared memory; the override ctas_per_sm = 2 sizes the grid for two,
+    // each with half of it.
+    const int dt_k = dtype == DL_BF16 ? dl::kBF16 : dl::kFP8;
+    const int fits = dl::host_min_blocks(dt_k, pl.family, pl.mt);
     const int cps_o = g_cps_override.load();
-    const int cps = cps_o > 0 ? cps_o : 1;
+    const int cps = cps_o ? cps_o : fits;
+    const bool half_smem = cps == 2;
     long long grid = (long long)di.sm_count * cps;
     const int mc = g_max_ctas_override.load();
     if (mc > 0 && grid > mc) grid = mc;
     if (grid > pl.units) grid = pl.units;
     if (grid < 1) grid = 1;
     pl.grid = (int)grid;
-    pl.q = pl.units / pl.grid;
-    pl.r = (int)(pl.units % pl.grid);
-    // Pipeline depth: as many stages as the shared memory of one CTA (out of
-    // `cps` resident per SM) holds.
+    // Segments (a fixed partition of the units; CTAs claim them dynamically and
+    // the fix-up sums them in segment order): a first wave of one segment per
+    // CTA holding about 5/8 of the units, then waves of `grid` segments, each
+    // covering about half of what is left, down to a minimum size that keeps
+    // the split tiles' partials cheap: at least 2 units, at most ~24 segments
+    // per tile, and partial bytes (M x 512 per segment) small next to the
+    // segment's weight bytes.
+    {
+        const long long G = pl.grid, U = pl.units;
+        long long min_seg = 2;
+        const long long by_tile = (pl.KB + 23) / 24;
+        const long long by_m = dtype == DL_BF16 ? (M + 3) / 4 : (M + 1) / 2;
+        if (by_tile > min_seg) min_seg = by_tile;
+        if (by_m > min_seg) min_seg = by_m;
+        long long s0 = (U * 5 / 8) / G;
+        if (s0 < 1) s0 = 1;
+        int w = 0;
+        pl.wave_seg0[0] = 0;
+        pl.wave_unit0[0] = 0;
+        pl.wave_size[0] = (int)s0;
+        long long seg = G, unit = G * s0;
+        ++w;
+        while (unit < U) {
+            const long long rem = U - unit;
+            long long size = rem / (2 * G);
+            if (size < min_seg) size = min_seg;
+            if (w == dl::kMaxWaves - 1) size = (rem + G - 1) / G;   // last wave takes the rest
+            long long count = (rem + size - 1) / size;
+            if (count > G) count = G;
+            pl.wave_seg0[w] = (int)seg;
+            pl.wave_unit0[w] = unit;
+            pl.wave_size[w] = (int)size;
+            seg += count;
+            unit += count * size;
+            ++w;
+        }
+        pl.n_waves = w;
+        pl.n_segments = (int)seg;
+        pl.wave_seg0[w] = (int)seg;
+    }
+    // Pipeline depth: as many stages as the shared-memory budget holds.
     int budget = di.smem_optin;
-    const int per_sm = di.smem_per_sm / cps - 1024;
+    const int per_sm = (half_smem ? di.smem_per_sm / 2 : di.smem_per_sm) - 1024;
     if (per_sm < budget) budget = per_sm;
-    const int stage = dl::host_stage_bytes(dtype == DL_BF16 ? dl::kBF16 : dl::kFP8, pl.mt);
+    const int dt = dt_k;
     int stages = kMaxStages;
-    while (stages > 2 && (size_t)stages * stage + dl::host_fixed_smem_bytes(pl.mt, stages) + 1024 >
-                             (size_t)budget)
-        --stages;
-    if ((size_t)stages * stage + dl::host_fixed_smem_bytes(pl.mt, stages) + 1024 > (size_t)budget)
+    while (stages > 2 && dl::host_smem_bytes(dt, pl.family, pl.mt, stages) > budget) --stages;
+    if (dl::host_smem_bytes(dt, pl.family, pl.mt, stages) > budget)
         return fail(DL_ERR_UNSUPPORTED_SHAPE, "not enough shared memory for two pipeline stages");
     pl.stages = stages;
-    pl.smem = (size_t)stages * stage + dl::host_fixed_smem_bytes(pl.mt, stages) + 1024;
-    pl.tickets_off = 0;
-    pl.partials_off = align_up((size_t)pl.n_tiles * sizeof(int), 256);
-    pl.ws_bytes = pl.partials_off + (size_t)pl.grid * 2 * pl.mtb * dl::kBN * sizeof(float);
+    pl.smem = (size_t)dl::host_smem_bytes(dt, pl.family, pl.mt, stages);
+    // Workspace: [claim counter, done counter | pad] [tickets] [partials].
+    pl.counter_off = 0;
+    pl.tickets_off = 256;
+    pl.partials_off = align_up(pl.tickets_off + (size_t)pl.n_tiles * sizeof(int), 256);
+    pl.ws_bytes = pl.partials_off + (size_t)pl.n_segments * 2 * pl.mtb * dl::kBN * sizeof(float);
     return DL_OK;
 }
 
@@ -240,7 +289,8 @@ dl_status validate(int dtype, int M, int N, int K, const void* x, const void* W,
 
 dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void* W,
                        const float* scales, const void* bias, void* y, float* y_f32,
-                       void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di) {
+                       void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di,
+                       bool early_weights) {
     Plan pl;
     dl_status s = make_plan(dtype, M, N, K, di, pl);
     if (s != DL_OK) return s;
@@ -256,6 +306,7 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.y = static_cast<uint16_t*>(y);
     p.y_f32 = y_f32;
     p.scales = scales;
+    p.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.counter_off);
     p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.tickets_off);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.partials_off);
     p.M = M;
@@ -263,9 +314,17 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.K = K;
     p.KB = pl.KB;
     p.n_tiles = pl.n_tiles;
-    p.q = pl.q;
-    p.r = pl.r;
+    p.units = pl.units;
+    p.n_segments = pl.n_segments;
+    p.n_waves = pl.n_waves;
+    for (int w = 0; w < dl::kMaxWaves; ++w) {
+        p.wave_seg0[w] = w <= pl.n_waves ? pl.wave_seg0[w] : 0;
+        p.wave_unit0[w] = w < pl.n_waves ? pl.wave_unit0[w] : 0;
+        p.wave_size[w] = w < pl.n_waves ? pl.wave_size[w] : 1;
+    }
+    p.wave_seg0[dl::kMaxWaves] = pl.wave_seg0[pl.n_waves];
     p.stages = pl.stages;
+    p.early_weights = early_weights ? 1 : 0;
     p.err = di.err_word;
     cudaError_t e = dtype == DL_BF16
         ? dl::launch_linear_bf16(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true)
@@ -331,7 +390,7 @@ dl_status dl_linear_bf16(const void* x, const void* W, const void* bias, void* y
     DeviceInfo di;
     if ((s = device_info(di)) != DL_OK) return s;
     s = launch_layer(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32, workspace, ws_bytes,
-                     static_cast<cudaStream_t>(stream), di);
+                     static_cast<cudaStream_t>(stream), di, false);
     return s == DL_OK ? ok() : s;
 }
 
@@ -344,7 +403,7 @@ dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* sca
     DeviceInfo di;
     if ((s = device_info(di)) != DL_OK) return s;
     s = launch_layer(DL_FP8_B128, M, N, K, x, Wq, scales, bias, y, y_f32, workspace, ws_bytes,
-                     static_cast<cudaStream_t>(stream), di);
+                     static_cast<cudaStream_t>(stream), di, false);
     return s == DL_OK ? ok() : s;
 }
 
@@ -380,8 +439,11 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
     auto enqueue_all = [&]() -> dl_status {
         for (int i = 0; i < n_layers; ++i) {
             const dl_layer& L = layers[i];
+            // Layers after the first follow one of this library's own kernels,
+            // which never writes weights: they may prefetch their first weight
+            // tiles while that kernel drains.
             dl_status r = launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y,
-                                       nullptr, workspace, ws_bytes, st, di);
+                                       nullptr, workspace, ws_bytes, st, di, i > 0);
             if (r != DL_OK) {
                 std::string m = g_err;
                 return fail(r, "layer %d: %s", i, m.c_str());

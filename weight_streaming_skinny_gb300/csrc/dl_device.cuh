@@ -13,6 +13,7 @@ namespace dl {
 constexpr unsigned kErrConsumerWait = 1u;
 constexpr unsigned kErrProducerWait = 2u;
 constexpr unsigned kErrDrainWait = 4u;
+constexpr unsigned kErrGroupWait = 8u;
 
 // Every device-side wait gives up after this long and reports an error bit.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -79,6 +80,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Let the next kernel on the stream (launched with programmatic stream
+// serialization) start now; it still waits for this grid's completion before
+// it touches anything this grid writes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the previous kernel on the stream has completed and its memory
+// operations are visible (returns at once when there is no such kernel).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
@@ -106,6 +122,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy whose completion is counted on an
+// mbarrier (the barrier's pending count is raised now and lowered when the
+// copy lands, so the phase cannot complete before it).
+__device__ __forceinline__ void cp_async_4_mbar(uint32_t dst, const void* src, uint32_t bar) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ---------------------------------------------------------------- shared loads
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -119,6 +143,10 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 v;
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
     return v;
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
@@ -145,27 +173,108 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A(16x16 f16, row) * B(16x8 f16, col) + C, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- warp reductions
+
+__device__ __forceinline__ unsigned warp_max_u32(unsigned v) {
+    unsigned r;
+    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+__device__ __forceinline__ unsigned warp_min_u32(unsigned v) {
+    unsigned r;
+    asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
 // ---------------------------------------------------------------- conversions
 
+// Four e4m3 codes (bytes 0..3 of `four`) to two f16x2: lo = (code0, code1),
+// hi = (code2, code3), low byte -> low half.  Exact for every code (E4M3FN
+// values are normal f16 numbers or zero; NaN codes become f16 NaN); one
+// conversion-pipe instruction per pair.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t"
+        ".reg .b16 c0, c1;\n\t"
+        "mov.b32 {c0, c1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c0;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, c1;\n\t"
+        "}"
+        : "=r"(lo), "=r"(hi) : "r"(four));
+}
+
+// Two fp32 to f16x2 (a -> low half), round to nearest even.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
 // Two e4m3 codes (low byte -> low half) to two bf16, exactly.  e4m3 -> f16 is
-// exact (every E4M3FN value is a normal f16 or zero, NaN stays NaN) and
-// f16 -> bf16 is exact for those values (3 significant bits, exponents
-// -9..8), so the composition is the exact decode.
+// exact (every E4M3FN value is a normal f16 or zero; NaN stays NaN), f16 ->
+// f32 is exact, and an f32 holding an e4m3 value has at most 4 significant
+// bits, so its upper 16 bits ARE the bf16 encoding: one byte-permute packs
+// the two upper halves.  Only the first step uses the conversion pipe.
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
     uint32_t out;
     asm("{\n\t"
-        ".reg .b16 c, lo, hi, blo, bhi;\n\t"
+        ".reg .b16 c, lo, hi;\n\t"
         ".reg .b32 h2;\n\t"
+        ".reg .f32 flo, fhi;\n\t"
         "cvt.u16.u32 c, %1;\n\t"
         "cvt.rn.f16x2.e4m3x2 h2, c;\n\t"
         "mov.b32 {lo, hi}, h2;\n\t"
-        "cvt.rn.bf16.f16 blo, lo;\n\t"
-        "cvt.rn.bf16.f16 bhi, hi;\n\t"
-        "mov.b32 %0, {blo, bhi};\n\t"
+        "cvt.f32.f16 flo, lo;\n\t"
+        "cvt.f32.f16 fhi, hi;\n\t"
+        "prmt.b32 %0, flo, fhi, 0x7632;\n\t"
         "}"
         : "=r"(out) : "r"(two_codes));
     return out;
 }
+
+// The same decode, exact for every code except the two NaN codes, with only
+// one instruction on the conversion pipe: e4m3 -> f16 (exact), then the f16
+// bits are re-packed as bf16 by integer ops -- magnitude shifted right by 3
+// (f16 exponent bits land in the bf16 exponent field, mantissa bits below it;
+// an e4m3 value has no low mantissa bits to lose), sign kept -- which encodes
+// value * 2^-112 (exponent bias 15 read as bias 127); a bf16x2 multiply by
+// 2^112 restores the value exactly (zero stays zero).  NaN codes come out
+// finite here, so `nan_guard` accumulates h * 0 in f16: it turns NaN as soon
+// as any NaN code was seen, and the caller then redoes its work with
+// e4m3x2_to_bf16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_fast(uint32_t two_codes, uint32_t& nan_guard) {
+    uint32_t out;
+    asm("{\n\t"
+        ".reg .b16 c;\n\t"
+        ".reg .b32 h2, t, u, zero, scale;\n\t"
+        "cvt.u16.u32 c, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h2, c;\n\t"
+        "mov.b32 zero, 0;\n\t"
+        "fma.rn.f16x2 %1, h2, zero, %1;\n\t"
+        "shr.b32 t, h2, 3;\n\t"
+        "and.b32 t, t, 0x0FFF0FFF;\n\t"
+        "and.b32 u, h2, 0x80008000;\n\t"
+        "or.b32 t, t, u;\n\t"
+        "mov.b32 scale, 0x77807780;\n\t"
+        "mul.rn.bf16x2 %0, t, scale;\n\t"
+        "}"
+        : "=r"(out), "+r"(nan_guard) : "r"(two_codes));
+    return out;
+}
+
+// True if a nan_guard accumulator saw a NaN code (either half non-zero).
+__device__ __forceinline__ bool nan_guard_tripped(uint32_t g) { return (g & 0x7fff7fffu) != 0u; }
 
 // acc + a.lo * b.lo, then + a.hi * b.hi: bf16 x bf16 products are exact in
 // fp32; each step is one fused multiply-add with a single rounding.
@@ -198,6 +307,19 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float v) {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Ticket increment with acquire-release semantics at GPU scope: publishes this
+// CTA's partial (ordered before by a CTA barrier) and, for the last arriver,
+// makes every earlier contributor's partial visible.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void st_cg_f32(float* p, float v) {
+    asm volatile("st.global.cg.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ float ld_cg_f32(const float* p) {

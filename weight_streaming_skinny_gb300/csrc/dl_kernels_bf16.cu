@@ -9,15 +9,12 @@ cudaError_t launch_linear_bf16(int family, int mt, const CUtensorMap& tw, const 
     return launch_family<kBF16>(family, mt, tw, tx, p, grid, smem, stream, launch);
 }
 
-int host_stage_bytes(int dtype, int mt) {
-    const int xr = mt < 8 ? 8 : mt;
-    return kBN * kBK * (dtype == kBF16 ? 2 : 1) + xr * kBK * 2;
+int host_smem_bytes(int dtype, int family, int mt, int stages) {
+    return smem_layout(dtype, family, mt, stages).total + 1024;   // + alignment slack
 }
 
 int host_x_rows(int mt) { return mt < 8 ? 8 : mt; }
 
-int host_fixed_smem_bytes(int mt, int stages) {
-    return host_x_rows(mt) * kRedStride * 4 + stages * 16 + 16;
-}
+int host_min_blocks(int dtype, int family, int mt) { return min_blocks_for(dtype, family, mt); }
 
 }  // namespace dl

@@ -29,7 +29,21 @@ cudaError_t launch_instance(const CUtensorMap& tw, const CUtensorMap& tx, const 
                             int grid, size_t smem, cudaStream_t stream, bool launch) {
     cudaError_t e = prepare_instance<DT, FAM, MT>(smem);
     if (e != cudaSuccess || !launch) return e;
-    linear_kernel<DT, FAM, MT><<<grid, kThreads, smem, stream>>>(tw, tx, p);
+    // Programmatic stream serialization: this grid may start while the
+    // previous kernel on the stream drains; the kernel orders every dependent
+    // access after griddepcontrol.wait.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads_for(DT, FAM));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, linear_kernel<DT, FAM, MT>, tw, tx, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -45,11 +59,15 @@ cudaError_t launch_family(int family, int mt, const CUtensorMap& tw, const CUten
     switch (mt) {
         case 1: return launch_instance<DT, kSIMT, 1>(tw, tx, p, grid, smem, stream, launch);
         case 2: return launch_instance<DT, kSIMT, 2>(tw, tx, p, grid, smem, stream, launch);
-        case 4: return launch_instance<DT, kSIMT, 4>(tw, tx, p, grid, smem, stream, launch);
-        case 8: return launch_instance<DT, kSIMT, 8>(tw, tx, p, grid, smem, stream, launch);
-        case 16: return launch_instance<DT, kSIMT, 16>(tw, tx, p, grid, smem, stream, launch);
-        default: return cudaErrorInvalidValue;
+        default: break;
     }
+    if constexpr (DT == kBF16) {
+        // FP8 SIMT stops at 2 tokens (the host plan switches to MMA beyond).
+        if (mt == 4) return launch_instance<DT, kSIMT, 4>(tw, tx, p, grid, smem, stream, launch);
+        if (mt == 8) return launch_instance<DT, kSIMT, 8>(tw, tx, p, grid, smem, stream, launch);
+        if (mt == 16) return launch_instance<DT, kSIMT, 16>(tw, tx, p, grid, smem, stream, launch);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace dl

@@ -11,11 +11,12 @@ namespace dl {
 
 struct LinearParams;
 
-// Shared-memory bytes of one pipeline stage and the per-CTA fixed part, for a
-// kernel staging `mt` token rows (mt in {1,2,4,8,16}).
-int host_stage_bytes(int dtype, int mt);
-int host_fixed_smem_bytes(int mt, int stages);
+// Dynamic shared memory of one CTA of the (dtype, family, mt) kernel with
+// `stages` pipeline stages, and the token rows it stages (mt in {1,2,4,8,16}).
+int host_smem_bytes(int dtype, int family, int mt, int stages);
 int host_x_rows(int mt);
+// CTAs per SM the (dtype, family, mt) kernel is compiled to fit.
+int host_min_blocks(int dtype, int family, int mt);
 
 // Launch the (dtype, family, mt) instance (launch = false: only raise its
 // shared-memory ceiling on the current device, which is done once per device
