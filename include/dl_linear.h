@@ -117,6 +117,45 @@ dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* sca
                                  const void* bias, void* y, float* y_f32, int M, int N,
                                  int K, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * Bytes of the library's static device scratch (see below): 16 MiB per device.
+ */
+#define DL_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * dl_linear_bf16 without a caller-supplied workspace: the split-K scratch is a
+ * file-scope device array of DL_STATIC_SCRATCH_BYTES inside the library, and
+ * neither this function nor anything it calls allocates device memory (no
+ * cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * Who needs it: code that may not allocate device memory of its own -- for
+ * instance a plugin running inside a host framework whose allocator owns the
+ * whole device-memory budget, or a latency-critical decode loop that must not
+ * call cudaMalloc/cudaFree because they can synchronise the device and stall
+ * every other stream.
+ *
+ * The pages that define the operation have no counterpart to this entry point;
+ * it is an interface convenience, computing exactly what dl_linear_bf16 does.
+ *
+ * Arguments: as for dl_linear_bf16, minus workspace/ws_bytes.
+ * Limits and errors: shapes whose work plan needs more than
+ *   DL_STATIC_SCRATCH_BYTES of scratch (dl_workspace_bytes(M, N, K, DL_BF16)
+ *   tells) are rejected with DL_ERR_WORKSPACE before anything is enqueued.  The
+ *   limit covers every Qwen2.5-72B decoder linear and the lm_head at M <= 8.
+ * Set-up: the first call on each device, with that device current, looks up
+ *   the array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture begins.
+ * Sharing: every call on a device uses the same array, which keeps what the
+ *   last call left.  Each call first clears (cudaMemsetAsync on `stream`) the
+ *   arrival counters that must start at zero; the partial sums need no
+ *   clearing.  Calls ordered on one stream are safe; calls that can overlap on
+ *   the GPU (other streams, other threads) race on the array and give wrong
+ *   results.  If the kernel launch itself fails (DL_ERR_CUDA), that clearing
+ *   may already be enqueued; it touches only the library's array.
+ */
+dl_status dl_linear_bf16_static_scratch(const void* x, const void* W, const void* bias, void* y,
+                                        float* y_f32, int M, int N, int K, void* stream);
+
 /* One layer of a decode weight stream (see dl_decode_stream). */
 typedef struct dl_layer {
     int dtype;             /* dl_dtype                                    */

@@ -1,0 +1,85 @@
+"""dl_linear_bf16_static_scratch: the entry point that allocates nothing and
+keeps its split-K state in the library's static device scratch.  Checked
+against dl_linear_bf16 (caller workspace) on calls issued back to back, so that
+each call starts from what the previous one left in the shared scratch.
+
+This file is collected last on purpose: it must pass in a fresh process (the
+first call on the device does the scratch set-up) and after every other test
+(the scratch and the overrides then carry earlier state)."""
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_streaming_skinny_gb300 as dl
+from weight_streaming_skinny_gb300 import inputs
+from parity_util import ABS_TOL, REL_TOL, oracle_for
+
+# (M, N, K, bias): split-K tiles with partial sums and a ragged tail; a second
+# shape with more tiles (its tickets lie over the first call's partials); the
+# first shape again.
+CALLS = [(1, 4096, 8192, True), (6, 1000, 2048, False), (1, 4096, 8192, True)]
+
+
+def _within_tolerance(y32, y32_ref, a, what):
+    g = y32.detach().cpu().double().numpy()
+    r = y32_ref.detach().cpu().double().numpy()
+    bound = REL_TOL * a + ABS_TOL
+    bad = ~(np.abs(g - r) <= bound)
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside tolerance"
+
+
+@pytest.mark.gpu
+def test_static_scratch_matches_workspace_entry_point(cuda_device):
+    dl.set_override(0, 0, 0)
+    host = [inputs.make_layer(inputs.DTYPE_BF16, M, N, K, bias=b, config_id=90 + (i % 2))
+            for i, (M, N, K, b) in enumerate(CALLS)]
+    dev = [L.to(cuda_device) for L in host]
+    for L in dev:
+        assert dl.workspace_bytes(L.M, L.N, L.K, dl.BF16) <= dl.STATIC_SCRATCH_BYTES
+    outs = [(torch.empty((L.M, L.N), dtype=torch.bfloat16, device=cuda_device),
+             torch.empty((L.M, L.N), dtype=torch.float32, device=cuda_device)) for L in dev]
+    # Back to back on one stream, no host synchronisation in between.
+    for L, (y, y32) in zip(dev, outs):
+        dl.linear_bf16_static_scratch(L.x, L.w, L.bias, out=y, out_f32=y32)
+    torch.cuda.synchronize(cuda_device)
+    assert dl.device_status() == 0
+
+    for i, (Lh, L, (y, y32)) in enumerate(zip(host, dev, outs)):
+        ws = dl.Workspace(dl.workspace_bytes(L.M, L.N, L.K, dl.BF16), cuda_device)
+        y32_ref = torch.empty_like(y32)
+        y_ref = dl.linear_bf16(L.x, L.w, L.bias, out_f32=y32_ref, workspace=ws)
+        torch.cuda.synchronize(cuda_device)
+        _, a = oracle_for(Lh)
+        _within_tolerance(y32, y32_ref, a, f"call {i} M={L.M} N={L.N} K={L.K}")
+        # y is y_f32 rounded once to nearest even
+        assert np.array_equal(oracle.round_to_bf16(y32.cpu().numpy()), inputs.bf16_bits(y))
+    # The third call repeats the first one's inputs after another shape used the
+    # scratch: same plan, same kernel, so the same bits.
+    assert torch.equal(outs[0][1], outs[2][1]) and torch.equal(outs[0][0], outs[2][0])
+
+
+@pytest.mark.gpu
+def test_static_scratch_rejects_oversize_plans(cuda_device):
+    dl.set_override(0, 0, 0)
+    K = 8192
+    for M, N in [(9, 59136), (16, 152064)]:
+        if dl.workspace_bytes(M, N, K, dl.BF16) > dl.STATIC_SCRATCH_BYTES:
+            break
+    else:
+        pytest.skip("no candidate shape needs more scratch than the limit on this device")
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device=cuda_device)
+    w = torch.zeros((N, K), dtype=torch.bfloat16, device=cuda_device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(dl.DLError) as e:
+        dl.linear_bf16_static_scratch(x, w, out=y)
+    assert e.value.status == 4
+    assert "static scratch" in str(e.value)
+
+
+def test_static_scratch_limit_matches_header():
+    text = open(dl._HEADER).read()
+    m = re.search(r"#define\s+DL_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m and (int(m.group(1)) << int(m.group(2))) == dl.STATIC_SCRATCH_BYTES

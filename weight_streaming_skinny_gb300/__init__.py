@@ -20,6 +20,7 @@ import torch
 __all__ = [
     "BF16", "FP8_B128", "KERNEL_AUTO", "KERNEL_SIMT", "KERNEL_MMA", "DLError", "Layer",
     "library_path", "load", "version", "workspace_bytes", "Workspace", "linear_bf16",
+    "linear_bf16_static_scratch", "STATIC_SCRATCH_BYTES",
     "linear_fp8_block128", "decode_stream", "graph_cache_clear", "set_override",
     "device_status", "exported_symbols", "header_symbols",
 ]
@@ -213,6 +214,40 @@ def linear_bf16(x, w, bias=None, *, out=None, out_f32=None, workspace: Workspace
         ws = _workspace(workspace, need, dev)
         _check(load().dl_linear_bf16(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), _ptr(out_f32),
                                      M, N, K, ws.ptr, ws.nbytes, _stream(stream, dev)))
+    return out
+
+
+STATIC_SCRATCH_BYTES = 16 << 20   # DL_STATIC_SCRATCH_BYTES of include/dl_linear.h
+
+
+def linear_bf16_static_scratch(x, w, bias=None, *, out, out_f32=None, stream=None):
+    """linear_bf16 through dl_linear_bf16_static_scratch: no workspace argument;
+    the library's static device scratch (STATIC_SCRATCH_BYTES per device) holds
+    the split-K state and nothing is allocated on the call path, so `out` (and
+    `out_f32`, if wanted) must be passed in.  Calls that may overlap on the GPU
+    share that scratch and race; calls ordered on one stream do not."""
+    if out is None:
+        raise ValueError("out is required: this entry point allocates nothing")
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    _need(w, "w", torch.bfloat16, dev)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, dev)
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("x must be [M, K] and w [N, K]")
+    M, K = x.shape
+    N = w.shape[0]
+    if bias is not None and bias.numel() != N:
+        raise ValueError("bias must be [N]")
+    out = _out(out, out_f32, M, N, dev)
+    lib = load()
+    fn = lib.dl_linear_bf16_static_scratch
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp]
+    fn.restype = i
+    with torch.cuda.device(dev):
+        _check(fn(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), _ptr(out_f32), M, N, K,
+                  _stream(stream, dev)))
     return out
 
 

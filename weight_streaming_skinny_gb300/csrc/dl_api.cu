@@ -22,6 +22,11 @@
 // Device error word: bounded waits in the kernels OR their bit in here.
 __device__ unsigned int g_dl_device_error = 0;
 
+// Scratch of dl_linear_bf16_static_scratch: the split-K workspace (counters,
+// arrival tickets, partial sums) for callers that cannot allocate one.  One
+// copy per device, shared by every call of that entry point.
+__device__ __align__(256) unsigned char g_dl_static_scratch[DL_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -349,6 +354,28 @@ dl_status prepare_layer(int dtype, int M, int N, int K, const DeviceInfo& di) {
     return DL_OK;
 }
 
+// Device address of g_dl_static_scratch on the current device, looked up once
+// per device (cudaGetSymbolAddress) and cached.
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+dl_status static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(DL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(DL_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dl_static_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(DL_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return DL_OK;
+}
+
 // ----------------------------------------------------------------- graph cache
 
 std::mutex g_graph_mu;
@@ -391,6 +418,31 @@ dl_status dl_linear_bf16(const void* x, const void* W, const void* bias, void* y
     if ((s = device_info(di)) != DL_OK) return s;
     s = launch_layer(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32, workspace, ws_bytes,
                      static_cast<cudaStream_t>(stream), di, false);
+    return s == DL_OK ? ok() : s;
+}
+
+dl_status dl_linear_bf16_static_scratch(const void* x, const void* W, const void* bias, void* y,
+                                        float* y_f32, int M, int N, int K, void* stream) {
+    dl_status s = validate(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32);
+    if (s != DL_OK) return s;
+    DeviceInfo di;
+    if ((s = device_info(di)) != DL_OK) return s;
+    Plan pl;
+    if ((s = make_plan(DL_BF16, M, N, K, di, pl)) != DL_OK) return s;
+    if (pl.ws_bytes > (size_t)DL_STATIC_SCRATCH_BYTES)
+        return fail(DL_ERR_WORKSPACE,
+                    "M=%d N=%d K=%d needs %zu bytes of scratch; the static scratch holds %zu "
+                    "(use dl_linear_bf16 with a workspace)",
+                    M, N, K, pl.ws_bytes, (size_t)DL_STATIC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    if ((s = static_scratch(&scratch)) != DL_OK) return s;
+    // The claim/done counters and the arrival tickets must start at zero; the
+    // partial slots are always written before they are read.
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, pl.partials_off, st);
+    if (e != cudaSuccess) return fail(DL_ERR_CUDA, "clearing the static scratch: %s", cudaGetErrorString(e));
+    s = launch_layer(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32, scratch,
+                     (size_t)DL_STATIC_SCRATCH_BYTES, st, di, false);
     return s == DL_OK ? ok() : s;
 }
 
