@@ -38,11 +38,15 @@
  *  - Shapes: 1 <= M <= 16; 1 <= N, K < 2^31; BF16 needs K % 8 == 0 and FP8
  *    needs K % 128 == 0 (else DL_ERR_UNSUPPORTED_SHAPE).  x and W/Wq must be
  *    16-byte aligned (DL_ERR_MISALIGNED); bias/y 2-byte, y_f32/scales 4-byte.
- *  - Workspace: a device buffer of at least dl_workspace_bytes(...) bytes,
- *    ZERO-FILLED ONCE before its first use.  Each call leaves it ready for the
- *    next (its arrival counters return to zero), so it never needs clearing
- *    again unless a call reported a device-side error.  Two calls that may run
- *    at the same time (different streams) must not share a workspace.
+ *  - Shapes also need N <= 2,097,152 (16,384 tiles of 128 rows).
+ *  - Workspace: a device buffer of at least dl_workspace_bytes(...) bytes
+ *    (256-byte aligned) whose first DL_WORKSPACE_ZERO_BYTES are ZERO-FILLED
+ *    ONCE before its first use: the arrival counters, which every call returns
+ *    to zero, so they never need clearing again unless a call reported a
+ *    device-side error.  The rest is scratch (split-K partial sums and, for
+ *    FP8, an f16 copy of x) that every call writes before it reads.  One
+ *    workspace serves calls of any shape in turn; two calls that may run at
+ *    the same time (different streams) must not share a workspace.
  *  - Results are deterministic: the same inputs, shape, device (SM count) and
  *    overrides give bitwise identical outputs on every call.
  */
@@ -57,6 +61,9 @@ extern "C" {
 #endif
 
 #define DL_VERSION 1
+
+/* Leading workspace bytes that must be zero before a call (see conventions). */
+#define DL_WORKSPACE_ZERO_BYTES (256u + 16384u * 4u)
 
 typedef enum dl_status {
     DL_OK = 0,
@@ -112,6 +119,9 @@ dl_status dl_linear_bf16(const void* x, const void* W, const void* bias, void* y
  * Each e4m3 code is decoded exactly (NaN codes 0x7F/0xFF decode to NaN); the
  * block scale multiplies the fp32 partial sum of each 128-wide K block, which
  * is algebraically the same as scaling every weight.
+ * Enqueues two kernels: an activation prep kernel (writes the exact f16 copy
+ * of x into the workspace) and the main kernel.  If the second launch fails
+ * (DL_ERR_CUDA), the first may have run; it writes only the workspace.
  */
 dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* scales,
                                  const void* bias, void* y, float* y_f32, int M, int N,
@@ -203,7 +213,8 @@ dl_status dl_set_override(int kernel, int ctas_per_sm, int max_ctas);
  * Read and clear the device error word of the current device: bit 0 = a
  * consumer gave up waiting for a weight tile, bit 1 = the loader gave up
  * waiting for a free stage, bit 2 = the final wait for copies in flight gave
- * up.  Every device wait is bounded (about 2 s); a kernel that gives up sets a
+ * up, bit 3 = a hand-over of a split-K run between the consumer warps and the
+ * ticket warp gave up.  Every device wait is bounded (about 2 s); a kernel that gives up sets a
  * bit and returns instead of hanging.  SYNCHRONISES the device.  *flags may
  * be NULL.  Returns DL_ERR_DEVICE if any bit was set.
  */

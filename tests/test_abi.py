@@ -112,3 +112,10 @@ def test_error_message_is_thread_local_and_cleared():
     assert lib.dl_set_override(0, 0, 0) == 0
     assert lib.dl_last_error() == b""
     assert ctypes.sizeof(dl._Layer) == 4 * 4 + 5 * 8
+
+
+def test_workspace_zero_prefix_matches_header():
+    import re
+    text = open(dl._HEADER).read()
+    m = re.search(r"#define\s+DL_WORKSPACE_ZERO_BYTES\s+\((\d+)u\s*\+\s*(\d+)u\s*\*\s*(\d+)u\)", text)
+    assert m and int(m.group(1)) + int(m.group(2)) * int(m.group(3)) == dl.WORKSPACE_ZERO_BYTES

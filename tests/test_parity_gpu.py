@@ -127,6 +127,26 @@ def test_e4m3_dequant_bit_exact_all_codes(cuda_device, family):
 
 
 @pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("M", [1, 2, 6, 16])
+def test_fp8_activations_not_exact_in_f16(cuda_device, family, M):
+    """FP8 units whose activation block spans more than f16 can hold after one
+    power-of-two scaling (here ~60 binades, and values below f16's reach) take
+    the exact bf16 route; the rest of the layer keeps the f16 route."""
+    dl.set_override(family, 0, 0)
+    N, K = 300, 1024
+    L = inputs.make_layer(inputs.DTYPE_FP8_B128, M, N, K, bias=True, config_id=47)
+    x = L.x.float()
+    x[0, 128 + 5] = 2.0 ** 40                    # token 0, block 1: huge and tiny values
+    x[0, 128 + 6] = -1.5 * 2.0 ** -20
+    x[M - 1, 3] = 2.0 ** -100                    # last token, block 0: far below the rest
+    x[M - 1, 700] = 3.0 * 2.0 ** 30              # and block 5: one large value
+    L.x = x.to(torch.bfloat16)
+    y, y32 = run_gpu(L.to(cuda_device), cuda_device)
+    ref, a = oracle_for(L)
+    assert_parity(y, y32, ref, a, what=f"fp8 wide-range x M={M} fam={family}")
+
+
+@pytest.mark.parametrize("family", FAMILIES)
 def test_one_hot_bf16_selects_column_exactly(cuda_device, family):
     dl.set_override(family, 0, 0)
     N, K = 300, 1024
@@ -229,8 +249,12 @@ def test_guard_bands_untouched(cuda_device, family):
         ybuf = torch.full((2 * G + M * N,), -7.0, dtype=torch.bfloat16, device=cuda_device)
         fbuf = torch.full((2 * G + M * N,), -7.0, dtype=torch.float32, device=cuda_device)
         need = dl.workspace_bytes(M, N, K, dl.BF16 if dtype == inputs.DTYPE_BF16 else dl.FP8_B128)
+        Z = dl.WORKSPACE_ZERO_BYTES
         wsbuf = torch.full((need + G,), 0xAB, dtype=torch.uint8, device=cuda_device)
-        wsbuf[:need] = 0
+        # zero prefix (counters, tickets); the scratch after it starts as NaN
+        # bytes, so a partial sum read before it was written would show
+        wsbuf[:Z] = 0
+        wsbuf[Z:need] = 0xFF
         ws = dl.Workspace.__new__(dl.Workspace)
         ws.nbytes, ws.tensor = need, wsbuf
         y = ybuf[G:G + M * N]
@@ -243,14 +267,17 @@ def test_guard_bands_untouched(cuda_device, family):
         assert torch.all(ybuf[:G] == -7.0) and torch.all(ybuf[G + M * N:] == -7.0)
         assert torch.all(fbuf[:G] == -7.0) and torch.all(fbuf[G + M * N:] == -7.0)
         assert torch.all(wsbuf[need:] == 0xAB)
-        # the whole workspace (tickets and partials) is back to zero after the call
-        assert torch.all(wsbuf[:need] == 0)
+        # the counters and tickets are back to zero after the call
+        assert torch.all(wsbuf[:Z] == 0)
+        ref, a = oracle_for(L)
+        assert_parity(y.view(M, N), y32.view(M, N), ref, a, what=f"guard bands {dtype} M={M} N={N}")
 
 
 @pytest.mark.parametrize("family", FAMILIES)
 def test_one_workspace_serves_calls_of_any_shape(cuda_device, family):
     """Calls with few tiles then many tiles share one workspace: every call leaves
-    it all-zero, so no call ever reads a stale arrival ticket."""
+    its zero prefix (counters, tickets) zero, so no call ever reads a stale
+    arrival ticket, and the scratch after it is written before it is read."""
     dl.set_override(family, 0, 0)
     shapes = [(inputs.DTYPE_BF16, 1, 300, 8192), (inputs.DTYPE_FP8_B128, 6, 640, 8192),
               (inputs.DTYPE_BF16, 2, 20000, 1024), (inputs.DTYPE_FP8_B128, 9, 30000, 1024),
@@ -264,7 +291,7 @@ def test_one_workspace_serves_calls_of_any_shape(cuda_device, family):
         rows = sample_rows(N, count=64, seed=i)
         ref, a = oracle_for(L, rows=rows)
         assert_parity(y, y32, ref, a, rows=rows, what=f"shared workspace call {i}")
-        assert torch.all(ws.tensor == 0), f"workspace not all-zero after call {i}"
+        assert torch.all(ws.tensor[:dl.WORKSPACE_ZERO_BYTES] == 0), f"zero prefix dirty after call {i}"
 
 
 def test_workspace_too_small_is_rejected_before_launch(cuda_device):

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "BF16", "FP8_B128", "KERNEL_AUTO", "KERNEL_SIMT", "KERNEL_MMA", "DLError", "Layer",
     "library_path", "load", "version", "workspace_bytes", "Workspace", "linear_bf16",
-    "linear_bf16_static_scratch", "STATIC_SCRATCH_BYTES",
+    "linear_bf16_static_scratch", "STATIC_SCRATCH_BYTES", "WORKSPACE_ZERO_BYTES",
     "linear_fp8_block128", "decode_stream", "graph_cache_clear", "set_override",
     "device_status", "exported_symbols", "header_symbols",
 ]
@@ -139,10 +139,10 @@ def workspace_bytes(M: int, N: int, K: int, dtype: int) -> int:
 
 
 class Workspace:
-    """A zero-filled device buffer for split-K partials and arrival tickets.
-
-    Zeroed once here; the kernels leave it ready for the next call.  Do not
-    share one Workspace between streams that may run at the same time.
+    """A device buffer for the arrival counters (its first WORKSPACE_ZERO_BYTES,
+    zero-filled here once; every call leaves them zero) and the calls' scratch
+    (split-K partial sums, the FP8 activation copy).  Do not share one
+    Workspace between streams that may run at the same time.
     """
 
     def __init__(self, nbytes: int, device="cuda"):
@@ -218,6 +218,7 @@ def linear_bf16(x, w, bias=None, *, out=None, out_f32=None, workspace: Workspace
 
 
 STATIC_SCRATCH_BYTES = 16 << 20   # DL_STATIC_SCRATCH_BYTES of include/dl_linear.h
+WORKSPACE_ZERO_BYTES = 256 + 16384 * 4   # DL_WORKSPACE_ZERO_BYTES: zero before the first call
 
 
 def linear_bf16_static_scratch(x, w, bias=None, *, out, out_f32=None, stream=None):

@@ -50,6 +50,13 @@ std::atomic<int> g_max_ctas_override{0};
 
 constexpr int kMaxStages = 16;
 constexpr int kMaxDevices = 64;
+// Workspace prefix that must be zero before a call (and is zero after it):
+// the claim/done counters, then one arrival ticket per tile.  Fixed in size,
+// so that no call's scratch (partials, FP8 activation copy) ever lies where
+// another call's tickets do.
+constexpr size_t kTicketsOff = 256;
+constexpr int kMaxTiles = 16384;
+static_assert(kTicketsOff + (size_t)kMaxTiles * 4 == DL_WORKSPACE_ZERO_BYTES, "zero prefix");
 
 struct DeviceInfo {
     bool ready = false;
@@ -98,7 +105,7 @@ struct Plan {
     int wave_size[dl::kMaxWaves];
     int stages;
     size_t smem;
-    size_t counter_off, tickets_off, partials_off, ws_bytes;
+    size_t counter_off, tickets_off, partials_off, xh_off, unscale_off, ws_bytes;
 };
 
 int auto_family(int dtype, int M) {
@@ -140,6 +147,8 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     pl.mtb = dl::host_x_rows(pl.mt);
     pl.KB = (K + dl::kBK - 1) / dl::kBK;
     pl.n_tiles = (N + dl::kBN - 1) / dl::kBN;
+    if (pl.n_tiles > kMaxTiles)
+        return fail(DL_ERR_UNSUPPORTED_SHAPE, "N=%d exceeds %d rows", N, kMaxTiles * dl::kBN);
     pl.units = (long long)pl.n_tiles * pl.KB;
     // Grid: persistent, `cps` CTAs per SM: by default one, with all of the
     // SM's shared memory; the override ctas_per_sm = 2 sizes the grid for two,
@@ -206,11 +215,20 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
         return fail(DL_ERR_UNSUPPORTED_SHAPE, "not enough shared memory for two pipeline stages");
     pl.stages = stages;
     pl.smem = (size_t)dl::host_smem_bytes(dt, pl.family, pl.mt, stages);
-    // Workspace: [claim counter, done counter | pad] [tickets] [partials].
+    // Workspace: [claim counter, done counter | pad] [tickets, fixed size]
+    // [partials] and for FP8 [f16 copy of x] [unscale factors]; only the
+    // first DL_WORKSPACE_ZERO_BYTES must be zero (and are left zero).
     pl.counter_off = 0;
-    pl.tickets_off = 256;
-    pl.partials_off = align_up(pl.tickets_off + (size_t)pl.n_tiles * sizeof(int), 256);
-    pl.ws_bytes = pl.partials_off + (size_t)pl.n_segments * 2 * pl.mtb * dl::kBN * sizeof(float);
+    pl.tickets_off = kTicketsOff;
+    pl.partials_off = DL_WORKSPACE_ZERO_BYTES;
+    size_t end = pl.partials_off + (size_t)pl.n_segments * 2 * pl.mtb * dl::kBN * sizeof(float);
+    pl.xh_off = pl.unscale_off = 0;
+    if (dtype == DL_FP8_B128) {
+        pl.xh_off = align_up(end, 256);
+        pl.unscale_off = align_up(pl.xh_off + (size_t)M * K * 2, 256);
+        end = pl.unscale_off + (size_t)pl.KB * dl::kUnscaleStride * sizeof(float);
+    }
+    pl.ws_bytes = end;
     return DL_OK;
 }
 
@@ -265,7 +283,9 @@ dl_status encode_maps(const Plan& pl, int M, int N, int K, const void* x, const 
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
         const cuuint32_t box[2] = {64, (cuuint32_t)pl.mtb};
-        r = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
+        r = enc(&tx,
+                pl.dtype == DL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                2, const_cast<void*>(x), dims, strides, box,
                 ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
@@ -304,13 +324,21 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     if (ws_bytes < pl.ws_bytes)
         return fail(DL_ERR_WORKSPACE, "workspace has %zu bytes, this call needs %zu", ws_bytes,
                     pl.ws_bytes);
+    // FP8: the kernel streams the exact f16 copy of x that the prep kernel
+    // writes into the workspace.
+    char* wsb = static_cast<char*>(ws);
+    uint16_t* xh = dtype == DL_FP8_B128 ? reinterpret_cast<uint16_t*>(wsb + pl.xh_off) : nullptr;
+    float* unscale = dtype == DL_FP8_B128 ? reinterpret_cast<float*>(wsb + pl.unscale_off) : nullptr;
     CUtensorMap tw, tx;
-    if ((s = encode_maps(pl, M, N, K, x, W, tw, tx)) != DL_OK) return s;
+    if ((s = encode_maps(pl, M, N, K, xh ? static_cast<const void*>(xh) : x, W, tw, tx)) != DL_OK)
+        return s;
     dl::LinearParams p;
     p.bias = static_cast<const uint16_t*>(bias);
     p.y = static_cast<uint16_t*>(y);
     p.y_f32 = y_f32;
     p.scales = scales;
+    p.x = static_cast<const uint16_t*>(x);
+    p.unscale = unscale;
     p.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.counter_off);
     p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.tickets_off);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.partials_off);
@@ -331,9 +359,22 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.stages = pl.stages;
     p.early_weights = early_weights ? 1 : 0;
     p.err = di.err_word;
-    cudaError_t e = dtype == DL_BF16
-        ? dl::launch_linear_bf16(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true)
-        : dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
+    cudaError_t e;
+    if (dtype == DL_BF16) {
+        e = dl::launch_linear_bf16(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
+    } else {
+        // The main kernel's attribute first (the only host-side step that can
+        // fail for it), then prep -> main.  The prep kernel lets main launch
+        // only after its own predecessor has completed and never writes
+        // weights or scales, so main may always prefetch weights early.
+        e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, false);
+        if (e == cudaSuccess)
+            e = dl::launch_prep_x(static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, stream);
+        if (e == cudaSuccess) {
+            p.early_weights = 1;
+            e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
+        }
+    }
     if (e != cudaSuccess) return fail(DL_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return DL_OK;
 }
@@ -439,7 +480,7 @@ dl_status dl_linear_bf16_static_scratch(const void* x, const void* W, const void
     // The claim/done counters and the arrival tickets must start at zero; the
     // partial slots are always written before they are read.
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(scratch, 0, pl.partials_off, st);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, pl.tickets_off + (size_t)pl.n_tiles * sizeof(int), st);
     if (e != cudaSuccess) return fail(DL_ERR_CUDA, "clearing the static scratch: %s", cudaGetErrorString(e));
     s = launch_layer(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32, scratch,
                      (size_t)DL_STATIC_SCRATCH_BYTES, st, di, false);

@@ -13,7 +13,7 @@ namespace dl {
 constexpr unsigned kErrConsumerWait = 1u;
 constexpr unsigned kErrProducerWait = 2u;
 constexpr unsigned kErrDrainWait = 4u;
-constexpr unsigned kErrGroupWait = 8u;
+constexpr unsigned kErrRunWait = 8u;     // split-run hand-over (ticket warp / consumers)
 
 // Every device-side wait gives up after this long and reports an error bit.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -122,11 +122,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
-// 4-byte asynchronous global -> shared copy whose completion is counted on an
-// mbarrier (the barrier's pending count is raised now and lowered when the
-// copy lands, so the phase cannot complete before it).
-__device__ __forceinline__ void cp_async_4_mbar(uint32_t dst, const void* src, uint32_t bar) {
+// Asynchronous global -> shared copies (4 or 16 bytes, both addresses aligned
+// to the size) and the barrier arrival that tracks them: the barrier's pending
+// count is raised at once and lowered when every earlier cp.async of this
+// thread has landed, so the phase cannot complete before they do.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
@@ -243,39 +251,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
     return out;
 }
 
-// The same decode, exact for every code except the two NaN codes, with only
-// one instruction on the conversion pipe: e4m3 -> f16 (exact), then the f16
-// bits are re-packed as bf16 by integer ops -- magnitude shifted right by 3
-// (f16 exponent bits land in the bf16 exponent field, mantissa bits below it;
-// an e4m3 value has no low mantissa bits to lose), sign kept -- which encodes
-// value * 2^-112 (exponent bias 15 read as bias 127); a bf16x2 multiply by
-// 2^112 restores the value exactly (zero stays zero).  NaN codes come out
-// finite here, so `nan_guard` accumulates h * 0 in f16: it turns NaN as soon
-// as any NaN code was seen, and the caller then redoes its work with
-// e4m3x2_to_bf16x2.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_fast(uint32_t two_codes, uint32_t& nan_guard) {
-    uint32_t out;
-    asm("{\n\t"
-        ".reg .b16 c;\n\t"
-        ".reg .b32 h2, t, u, zero, scale;\n\t"
-        "cvt.u16.u32 c, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 h2, c;\n\t"
-        "mov.b32 zero, 0;\n\t"
-        "fma.rn.f16x2 %1, h2, zero, %1;\n\t"
-        "shr.b32 t, h2, 3;\n\t"
-        "and.b32 t, t, 0x0FFF0FFF;\n\t"
-        "and.b32 u, h2, 0x80008000;\n\t"
-        "or.b32 t, t, u;\n\t"
-        "mov.b32 scale, 0x77807780;\n\t"
-        "mul.rn.bf16x2 %0, t, scale;\n\t"
-        "}"
-        : "=r"(out), "+r"(nan_guard) : "r"(two_codes));
-    return out;
-}
-
-// True if a nan_guard accumulator saw a NaN code (either half non-zero).
-__device__ __forceinline__ bool nan_guard_tripped(uint32_t g) { return (g & 0x7fff7fffu) != 0u; }
-
 // acc + a.lo * b.lo, then + a.hi * b.hi: bf16 x bf16 products are exact in
 // fp32; each step is one fused multiply-add with a single rounding.
 __device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc) {
@@ -296,6 +271,41 @@ __device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc) {
         : "=f"(d) : "r"(a), "r"(b), "f"(acc));
     return d;
 #endif
+}
+
+// acc + a.lo * b.lo, then + a.hi * b.hi for f16 pairs: f16 x f16 products are
+// exact in fp32; each step is one fused multiply-add with a single rounding.
+__device__ __forceinline__ float fma2_f16(uint32_t a, uint32_t b, float acc) {
+    float d;
+    asm("{\n\t"
+        ".reg .b16 al, ah, bl, bh;\n\t"
+        ".reg .f32 t;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 t, al, bl, %3;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, t;\n\t"
+        "}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(acc));
+    return d;
+}
+
+// Global loads of 8 / 16 bytes (plain, coherent: the data may have been
+// written by the previous kernel on the stream).
+__device__ __forceinline__ uint2 ldg64(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg128(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg64(void* p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
 // fp32 -> bf16 bits, round to nearest even (NaN stays NaN).

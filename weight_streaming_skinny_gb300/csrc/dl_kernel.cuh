@@ -18,41 +18,48 @@
 // Pipeline.  Warp 8 (one elected thread) streams units HBM -> shared memory
 // with TMA tensor copies into a ring of `stages` buffers guarded by full/empty
 // mbarriers; each buffer carries a header naming its unit (and, for FP8, the
-// unit's block scale, copied asynchronously on the same barrier).  The weight
-// tile is copied as 128 rows x 128 bytes with the 128-byte swizzle.  Warps 0-7
-// each own 16 weight rows of the tile (the TileLang loop's T.Pipelined(...,
-// num_stages=2), deepened to cover GB300's HBM latency).  Every weight byte is
-// read from HBM exactly once per call.
+// unit's block scale and the per-token unscale factors of its activations,
+// copied asynchronously on the same barrier).  The weight tile is copied as
+// 128 rows x 128 bytes with the 128-byte swizzle.  Warps 0-7 each own 16
+// weight rows of the tile (the TileLang loop's T.Pipelined(..., num_stages=2),
+// deepened to cover GB300's HBM latency).  Every weight byte is read from HBM
+// exactly once per call.
+//
+// FP8 activations.  Before the main kernel, a prep kernel (dl_kernels_fp8.cu)
+// writes a copy of x in f16, each (token, 128-column block) scaled by a power of two chosen so
+// that the copy is exact, and the power of two that undoes it (0 when no such
+// power exists).  e4m3 codes convert exactly to f16 in one hardware
+// instruction per pair, so FP8 units multiply f16 weights by f16 activations
+// with fp32 accumulation, and the unscale factor and the block scale are
+// applied to each block's fp32 partial.  A unit whose activations are not
+// exact in f16 (rare: a block spanning more than ~32 binades, or inf/NaN)
+// runs the same products from the bf16 x in global memory with an exact
+// e4m3 -> bf16 decode.
 //
 // Consumer families:
 //   SIMT: one weight row per lane (two lanes per row, one per K half), CUDA-core
-//         fused multiply-adds with bf16 x bf16 -> fp32 products (the row-tiled
-//         GEMV of "Developing a custom Qwen2.5 72B inference engine from
-//         scratch", §6.1); a shuffle joins the two halves at the end of a run.
+//         mixed-precision fused multiply-adds (bf16 x bf16 or f16 x f16 ->
+//         fp32; the row-tiled GEMV of "Developing a custom Qwen2.5 72B
+//         inference engine from scratch", §6.1); a shuffle joins the two
+//         halves at the end of a run.
 //   MMA:  warp-level mma.sync m16n8k16 -> fp32 with the weights as the 16-row A
 //         operand and the (<= 16) tokens as the B operand (the
-//         "T.gemm(A_s, B_h, acc, transpose_B=True)" of the TileLang loop).
-//         bf16 weights feed a bf16 MMA directly.  FP8 weights are decoded by
-//         the hardware e4m3 -> f16 convert (exact) and multiplied, in an f16
-//         MMA, with a copy of x scaled by a power of two per (token, unit) so
-//         that it is exact in f16; the power of two is removed from the fp32
-//         partial.  Consumer warp w makes that copy for token w of the next
-//         stage while the current one is consumed.  Units whose x cannot be
-//         represented that way run the same products in a bf16 MMA instead.
+//         "T.gemm(A_s, B_h, acc, transpose_B=True)" of the TileLang loop), in
+//         bf16 for bf16 weights and in f16 for FP8 weights.
 // Two accumulator sets alternate over the K steps (shorter dependency chains);
-// they are added in a fixed order.  The fp32 block scale multiplies each
-// 128-wide K block's fp32 partial.
+// they are added in a fixed order.
 //
 // Split-K fix-up.  Within one segment the units of one tile form a "run".  A
 // run that covers its whole tile is finished on the spot: every warp rounds
 // its own rows (+ bias) to bf16 and stores them.  Otherwise the warps store
 // their fp32 partial rows in the workspace slot of the run's (segment,
-// first-or-last tile) pair; after a CTA barrier one thread takes the tile's
-// arrival ticket with an acquire-release atomic, whose result is looked at
-// only at the next run end (or exit), so its latency overlaps the next units.
-// The last run to arrive then has all warps sum the tile's slots in segment
-// order (= ascending K), add the bias, round once and zero the slots and the
-// ticket.  No CTA ever waits for another, and the order of every sum is fixed
+// first-or-last tile) pair and arrive on a barrier; a ticket warp (warp 9)
+// waits for all eight, then takes the tile's arrival ticket with an
+// acquire-release atomic -- the memory fence it implies stalls only that warp
+// -- and publishes whether this was the last contribution.  The consumers read
+// that result at their next split run end (or exit), long after it is ready;
+// if the tile is complete, all of them sum its slots in segment order (=
+// ascending K), add the bias, round once and reset the ticket.  No CTA ever waits for another, and the order of every sum is fixed
 // by the partition alone, so results are bitwise reproducible whichever CTA
 // computed which segment.  Inside one GPU this plays the role of the
 // row-parallel "partial sums, then all-reduce" of "Multi-GPU Inference and
@@ -62,10 +69,11 @@
 // soon as it starts (griddepcontrol.launch_dependents); all its threads but
 // the loader sleep in griddepcontrol.wait until the previous kernel has
 // finished, and the loader touches nothing that kernel may have written before
-// that wait -- except, when `early_weights` is set (a later layer of one
-// dl_decode_stream call, whose predecessor is this same kernel and never
-// writes weights or scales), the weight tiles and scales of its first stages,
-// which it prefetches while the previous layer drains.
+// that wait -- except, when `early_weights` is set (the previous kernel is
+// known never to write weights or scales: this kernel for an earlier layer of
+// one dl_decode_stream call, or the activation prep kernel, which itself
+// waits for its predecessor before it lets this one launch), the weight tiles
+// and scales of its first stages, which it prefetches meanwhile.
 //
 // Every wait is bounded (mbarrier waits give up after ~2 s, set a bit of the
 // device error word and make the CTA leave in an orderly way).
@@ -79,8 +87,11 @@ constexpr int kBN = 128;                 // weight rows per tile
 constexpr int kBK = 128;                 // K columns per unit (one FP8 scale block)
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kLoaderWarp = kConsumerWarps;       // warp 8: TMA producer
+constexpr int kTicketWarp = kConsumerWarps + 1;   // warp 9: split-K arrival tickets
+constexpr int kThreads = kConsumerThreads + 64;
 constexpr int kMaxWaves = 24;
+constexpr int kUnscaleStride = 16;       // unscale factors per k-block (one per token slot)
 
 enum DType { kBF16 = 0, kFP8 = 1 };
 enum Family { kSIMT = 1, kMMA = 2 };
@@ -95,9 +106,11 @@ struct LinearParams {
     uint16_t* y;              // bf16 [M][N]
     float* y_f32;             // fp32 [M][N] or null
     const float* scales;      // fp32 [ceil(N/128)][KB] (FP8)
+    const uint16_t* x;        // bf16 [M][K] (FP8: read only by units not exact in f16)
+    const float* unscale;     // fp32 [KB][16] (FP8): 2^-s of the f16 copy, 0 = not exact
     int* counter;             // [0]: segments claimed after the first wave, [1]: CTAs done
     int* tickets;             // [n_tiles] arrival counters (zero between calls)
-    float* partials;          // [n_segments][2][MTB][kBN] fp32 (zero between calls)
+    float* partials;          // [n_segments][2][MTB][kBN] fp32 (scratch)
     int M, N, K;
     int KB;                   // k-blocks per tile = ceil(K / 128)
     int n_tiles;
@@ -119,7 +132,9 @@ struct StageHeader {
     int flags;                // kRunFirst | kRunLast | kDone
     float scale;              // FP8 block scale of the unit (copied asynchronously)
     int pad[3];
+    float unscale[kUnscaleStride];   // FP8: per-token unscale factors of the k-block
 };
+static_assert(sizeof(StageHeader) == 96, "stage header layout");
 
 template <int DT>
 struct TileBytes {
@@ -134,29 +149,33 @@ struct XRows {
 // Shared-memory layout of one CTA (offsets from a 1024-aligned base).  The
 // host sizes the launch with the same function.
 struct SmemLayout {
-    int w, x, xh, hdr, unscale, bad, bars, flags, total;
+    int w, x, hdr, bars, runs, total;
 };
 
-__host__ __device__ constexpr SmemLayout smem_layout(int dtype, int family, int mt, int stages) {
+// Hand-over of one split run between the consumer warps and the ticket warp
+// (two slots, used alternately).
+struct RunSlot {
+    int tile;                 // tile of the run (-1: no more runs)
+    int jf, jl;               // first and last segment contributing to the tile
+    int last;                 // ticket result: tile if this run completed it, else -1
+};
+
+__host__ __device__ constexpr SmemLayout smem_layout(int dtype, int, int mt, int stages) {
     const int mtb = mt < 8 ? 8 : mt;
     const int wbytes = kBN * kBK * (dtype == kBF16 ? 2 : 1);
     const int xbytes = mtb * kBK * 2;
-    const bool half_x = (dtype == kFP8 && family == kMMA);
     SmemLayout L{};
     L.w = 0;
     L.x = L.w + stages * wbytes;
-    L.xh = L.x + stages * xbytes;
-    L.hdr = L.xh + (half_x ? stages * xbytes : 0);
-    L.unscale = L.hdr + stages * 32;
-    L.bad = L.unscale + (half_x ? stages * 16 * 4 : 0);
-    L.bars = L.bad + (half_x ? stages * 16 : 0);
-    L.flags = L.bars + (3 * stages + 1) * 8;
-    L.total = L.flags + 16;
+    L.hdr = L.x + stages * xbytes;
+    L.bars = L.hdr + stages * (int)sizeof(StageHeader);
+    L.runs = L.bars + (2 * stages + 4) * 8;
+    L.total = L.runs + 2 * (int)sizeof(RunSlot) + 16;
     return L;
 }
 
-// Threads of a CTA: 8 consumer warps and the loader warp.
-__host__ __device__ constexpr int threads_for(int, int) { return kConsumerThreads + 32; }
+// Threads of a CTA: 8 consumer warps, the loader warp and the ticket warp.
+__host__ __device__ constexpr int threads_for(int, int) { return kThreads; }
 
 // CTAs per SM an instance is compiled for: one, with the whole register file
 // and shared memory of the SM.  (A grid of two CTAs per SM can still be asked
@@ -215,8 +234,10 @@ struct SimtConsumer {
         for (int m = 0; m < MT; ++m) acc[0][m] = acc[1][m] = 0.f;
     }
 
-    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, uint32_t, const float*, bool,
-                                            int warp, int lane, float scale) {
+    // sw: weight tile of the stage; sx: activations of the stage (bf16, or for
+    // FP8 the exact f16 copy); hd: the stage header.
+    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, const StageHeader& hd,
+                                            const LinearParams& p, int warp, int lane) {
         const int row = warp * 16 + (lane & 15);
         const int h = lane >> 4;
         const int sw8 = row & 7;
@@ -238,45 +259,86 @@ struct SimtConsumer {
                 }
             }
         } else {
-            float part[2][MT];
-            uint32_t guard = 0;
-            fp8_unit<false>(sw, xbase, row, h, sw8, part, guard);
-            // A NaN code anywhere in the warp's unit: redo it with the decode
-            // that keeps NaN (never taken for clamped weights).
-            if (__any_sync(0xffffffffu, nan_guard_tripped(guard)))
-                fp8_unit<true>(sw, xbase, row, h, sw8, part, guard);
+            float u[MT];
+            bool exact = true;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[0][m] = fmaf(part[0][m] + part[1][m], scale, acc[0][m]);
+            for (int m = 0; m < MT; ++m) {
+                u[m] = hd.unscale[m];
+                exact &= (u[m] != 0.f);      // token slots >= M carry 1
+            }
+            float part[2][MT];
+            if (exact) {
+                fp8_unit_f16(sw, xbase, row, h, sw8, part);
+            } else {
+                fp8_unit_exact(sw, p, hd.kb, row, h, sw8, part);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) u[m] = 1.f;
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                acc[0][m] = fmaf((part[0][m] + part[1][m]) * u[m], hd.scale, acc[0][m]);
         }
     }
 
-    template <bool kExactNaN>
-    __device__ __forceinline__ void fp8_unit(uint32_t sw, uint32_t xbase, int row, int h, int sw8,
-                                             float (&part)[2][MT], uint32_t& guard) {
+    // One FP8 unit against the exact f16 copy of x: codes 16cc..16cc+15 of the
+    // row (cc = 4h + j) pair with f16 chunks 2j, 2j+1 of x box h.
+    __device__ __forceinline__ void fp8_unit_f16(uint32_t sw, uint32_t xbase, int row, int h,
+                                                 int sw8, float (&part)[2][MT]) {
         const uint32_t wbase = sw + row * 128;
 #pragma unroll
         for (int m = 0; m < MT; ++m) part[0][m] = part[1][m] = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int cc = 4 * h + j;                  // 16-code chunk of the row
+            const int cc = 4 * h + j;
+            const uint4 w = lds128(wbase + ((cc ^ sw8) << 4));
+            uint32_t wh[8];
+            e4m3x4_to_f16x2x2(w.x, wh[0], wh[1]);
+            e4m3x4_to_f16x2x2(w.y, wh[2], wh[3]);
+            e4m3x4_to_f16x2x2(w.z, wh[4], wh[5]);
+            e4m3x4_to_f16x2x2(w.w, wh[6], wh[7]);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint4 x0 = lds128(xbase + m * 128 + (((2 * j) ^ (m & 7)) << 4));
+                const uint4 x1 = lds128(xbase + m * 128 + (((2 * j + 1) ^ (m & 7)) << 4));
+                float a = part[j & 1][m];
+                a = fma2_f16(wh[0], x0.x, a);
+                a = fma2_f16(wh[1], x0.y, a);
+                a = fma2_f16(wh[2], x0.z, a);
+                a = fma2_f16(wh[3], x0.w, a);
+                a = fma2_f16(wh[4], x1.x, a);
+                a = fma2_f16(wh[5], x1.y, a);
+                a = fma2_f16(wh[6], x1.z, a);
+                a = fma2_f16(wh[7], x1.w, a);
+                part[j & 1][m] = a;
+            }
+        }
+    }
+
+    // The same unit from the bf16 x in global memory with the exact e4m3 ->
+    // bf16 decode (NaN codes stay NaN), for activations not exact in f16.
+    __device__ __forceinline__ void fp8_unit_exact(uint32_t sw, const LinearParams& p, int kb,
+                                                   int row, int h, int sw8, float (&part)[2][MT]) {
+        const uint32_t wbase = sw + row * 128;
+        const uint16_t* xk = p.x + (long long)kb * kBK + 64 * h;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[0][m] = part[1][m] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int cc = 4 * h + j;
             const uint4 w = lds128(wbase + ((cc ^ sw8) << 4));
             const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
             uint32_t wb[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if constexpr (kExactNaN) {
-                    wb[2 * i] = e4m3x2_to_bf16x2(wq[i] & 0xffffu);
-                    wb[2 * i + 1] = e4m3x2_to_bf16x2(wq[i] >> 16);
-                } else {
-                    wb[2 * i] = e4m3x2_to_bf16x2_fast(wq[i] & 0xffffu, guard);
-                    wb[2 * i + 1] = e4m3x2_to_bf16x2_fast(wq[i] >> 16, guard);
-                }
+                wb[2 * i] = e4m3x2_to_bf16x2(wq[i] & 0xffffu);
+                wb[2 * i + 1] = e4m3x2_to_bf16x2(wq[i] >> 16);
             }
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                // codes 16cc..16cc+15 pair with bf16 chunks 2j, 2j+1 of x box h
-                const uint4 x0 = lds128(xbase + m * 128 + (((2 * j) ^ (m & 7)) << 4));
-                const uint4 x1 = lds128(xbase + m * 128 + (((2 * j + 1) ^ (m & 7)) << 4));
+                if (m >= p.M) continue;
+                const uint16_t* xm = xk + (long long)m * p.K + 16 * j;
+                const uint4 x0 = ldg128(xm);
+                const uint4 x1 = ldg128(xm + 8);
                 float a = part[j & 1][m];
                 a = fma2_bf16(wb[0], x0.x, a);
                 a = fma2_bf16(wb[1], x0.y, a);
@@ -323,12 +385,8 @@ struct MmaConsumer {
                 for (int i = 0; i < 4; ++i) acc[k][nt][i] = 0.f;
     }
 
-    // sx: bf16 x tile of the stage; sxh: the same tile scaled exactly into
-    // f16 (FP8 only); xunscale[tok]: the power of two that undoes the
-    // scaling; exact_bf16: x of this unit is not exact in f16.
-    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, uint32_t sxh,
-                                            const float* xunscale, bool exact_bf16, int warp,
-                                            int lane, float scale) {
+    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, const StageHeader& hd,
+                                            const LinearParams& p, int warp, int lane) {
         const int mat = lane >> 3, rr = lane & 7;
         const int arow = warp * 16 + rr + ((mat & 1) << 3);
         const int aswz = arow & 7;
@@ -365,36 +423,40 @@ struct MmaConsumer {
                 }
             }
         } else {
-            float part[2][NT][4];
             const int t = lane & 3;
-            if (!exact_bf16) {
-                fp8_unit_f16(abase, aswz, mat, sxh, lane, part);
-            } else {
-                uint32_t guard = 0;
-                fp8_unit_bf16<false>(abase, aswz, mat, sx, lane, part, guard);
-                if (__any_sync(0xffffffffu, nan_guard_tripped(guard)))
-                    fp8_unit_bf16<true>(abase, aswz, mat, sx, lane, part, guard);
-            }
+            float u0[NT], u1[NT];
+            bool exact = true;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                // f16 path: part was computed against x * 2^k; undo the (exact)
-                // power of two, then apply the block scale.
-                const float u0 = exact_bf16 ? 1.f : xunscale[8 * nt + 2 * t];
-                const float u1 = exact_bf16 ? 1.f : xunscale[8 * nt + 2 * t + 1];
-                acc[0][nt][0] = fmaf((part[0][nt][0] + part[1][nt][0]) * u0, scale, acc[0][nt][0]);
-                acc[0][nt][1] = fmaf((part[0][nt][1] + part[1][nt][1]) * u1, scale, acc[0][nt][1]);
-                acc[0][nt][2] = fmaf((part[0][nt][2] + part[1][nt][2]) * u0, scale, acc[0][nt][2]);
-                acc[0][nt][3] = fmaf((part[0][nt][3] + part[1][nt][3]) * u1, scale, acc[0][nt][3]);
+                u0[nt] = hd.unscale[8 * nt + 2 * t];
+                u1[nt] = hd.unscale[8 * nt + 2 * t + 1];
+                exact &= (u0[nt] != 0.f) && (u1[nt] != 0.f);   // token slots >= M carry 1
+            }
+            float part[2][NT][4];
+            if (__all_sync(0xffffffffu, exact)) {
+                fp8_unit_f16(abase, aswz, mat, sx, lane, part);
+            } else {
+                fp8_unit_exact(abase, aswz, mat, p, hd.kb, lane, part);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) u0[nt] = u1[nt] = 1.f;
+            }
+            const float scale = hd.scale;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                acc[0][nt][0] = fmaf((part[0][nt][0] + part[1][nt][0]) * u0[nt], scale, acc[0][nt][0]);
+                acc[0][nt][1] = fmaf((part[0][nt][1] + part[1][nt][1]) * u1[nt], scale, acc[0][nt][1]);
+                acc[0][nt][2] = fmaf((part[0][nt][2] + part[1][nt][2]) * u0[nt], scale, acc[0][nt][2]);
+                acc[0][nt][3] = fmaf((part[0][nt][3] + part[1][nt][3]) * u1[nt], scale, acc[0][nt][3]);
             }
         }
     }
 
     // One FP8 unit (this warp's 16 rows x 128 codes) as an f16 MMA against the
-    // scaled f16 copy of x.  Step s is the 16-code chunk s of each row.  Thread
+    // exact f16 copy of x.  Step s is the 16-code chunk s of each row.  Thread
     // (g, t) receives codes 4t..4t+3 of its rows' chunk; they stand for
     // fragment columns {2t, 2t+1} and {2t+8, 2t+9}, so its B fragment is
     // x[token][16s + 4t .. 16s + 4t + 3], 8 bytes of the swizzled x box.
-    __device__ __forceinline__ void fp8_unit_f16(uint32_t abase, int aswz, int mat, uint32_t sxh,
+    __device__ __forceinline__ void fp8_unit_f16(uint32_t abase, int aswz, int mat, uint32_t sx,
                                                  int lane, float (&part)[2][NT][4]) {
         const int g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -413,7 +475,7 @@ struct MmaConsumer {
                 uint32_t A0, A1, A2, A3;
                 e4m3x4_to_f16x2x2(q[2 * ss], A0, A2);       // row g
                 e4m3x4_to_f16x2x2(q[2 * ss + 1], A1, A3);   // row g + 8
-                const uint32_t xbox = sxh + (step >> 2) * (MT * 128);
+                const uint32_t xbox = sx + (step >> 2) * (MT * 128);
                 const int xc = 2 * (step & 3) + (t >> 1);   // logical 16-byte chunk
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -425,11 +487,12 @@ struct MmaConsumer {
         }
     }
 
-    // The same products in a bf16 MMA against x as given, for units whose x is
-    // not exact in f16.  kExactNaN selects the decode that keeps NaN codes.
-    template <bool kExactNaN>
-    __device__ __forceinline__ void fp8_unit_bf16(uint32_t abase, int aswz, int mat, uint32_t sx,
-                                                  int lane, float (&part)[2][NT][4], uint32_t& guard) {
+    // The same products as a bf16 MMA with the exact e4m3 -> bf16 decode (NaN
+    // codes stay NaN) against the bf16 x in global memory, for activations
+    // not exact in f16.  Same K permutation as fp8_unit_f16.
+    __device__ __forceinline__ void fp8_unit_exact(uint32_t abase, int aswz, int mat,
+                                                   const LinearParams& p, int kb, int lane,
+                                                   float (&part)[2][NT][4]) {
         const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int k = 0; k < 2; ++k)
@@ -437,6 +500,7 @@ struct MmaConsumer {
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) part[k][nt][i] = 0.f;
+        const uint16_t* xk = p.x + (long long)kb * kBK + 4 * t;
 #pragma unroll 1
         for (int s = 0; s < 8; s += 2) {
             uint32_t q[4];
@@ -445,24 +509,15 @@ struct MmaConsumer {
             for (int ss = 0; ss < 2; ++ss) {
                 const int step = s + ss;
                 const uint32_t rlo = q[2 * ss], rhi = q[2 * ss + 1];
-                uint32_t A0, A1, A2, A3;
-                if constexpr (kExactNaN) {
-                    A0 = e4m3x2_to_bf16x2(rlo & 0xffffu);
-                    A2 = e4m3x2_to_bf16x2(rlo >> 16);
-                    A1 = e4m3x2_to_bf16x2(rhi & 0xffffu);
-                    A3 = e4m3x2_to_bf16x2(rhi >> 16);
-                } else {
-                    A0 = e4m3x2_to_bf16x2_fast(rlo & 0xffffu, guard);
-                    A2 = e4m3x2_to_bf16x2_fast(rlo >> 16, guard);
-                    A1 = e4m3x2_to_bf16x2_fast(rhi & 0xffffu, guard);
-                    A3 = e4m3x2_to_bf16x2_fast(rhi >> 16, guard);
-                }
-                const uint32_t xbox = sx + (step >> 2) * (MT * 128);
-                const int xc = 2 * (step & 3) + (t >> 1);
+                const uint32_t A0 = e4m3x2_to_bf16x2(rlo & 0xffffu);
+                const uint32_t A2 = e4m3x2_to_bf16x2(rlo >> 16);
+                const uint32_t A1 = e4m3x2_to_bf16x2(rhi & 0xffffu);
+                const uint32_t A3 = e4m3x2_to_bf16x2(rhi >> 16);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int tok = g + 8 * nt;
-                    const uint2 xb = lds64(xbox + tok * 128 + ((xc ^ (tok & 7)) << 4) + ((t & 1) << 3));
+                    const uint2 xb = tok < p.M ? ldg64(xk + (long long)tok * p.K + 16 * step)
+                                               : make_uint2(0u, 0u);
                     mma_bf16_16816(part[ss][nt], A0, A1, A2, A3, xb.x, xb.y);
                 }
             }
@@ -494,64 +549,14 @@ struct ConsumerOf<DT, kMMA, MT> {
     using type = MmaConsumer<DT, MT>;
 };
 
-// Rescale one token's 128 bf16 x values of a unit exactly into f16 (FP8 MMA
-// path).  Warp-cooperative: lane l converts 4 values in place of the
-// swizzled tile layout (box l/16, 8 bytes at element (l%16)*4).  With e the
-// largest biased exponent of the token's values, x * 2^(141 - e) has its
-// largest magnitude in [2^14, 2^15); every value then fits f16 exactly if no
-// non-zero value has a biased exponent below e - 31 (f16 subnormals keep 8
-// significant bits down to 2^-17) and none is an infinity or NaN.  Writes the
-// f16 values to sxh, 2^(e - 141) to *unscale and returns false when the
-// token is not exact in f16.
-template <int MTB>
-__device__ __forceinline__ bool scale_token_to_f16(uint32_t sx, uint32_t sxh, int tok, int lane,
-                                                   float* unscale) {
-    const uint32_t off = (lane >> 4) * (MTB * 128) + tok * 128 +
-                         ((((lane & 15) >> 1) ^ (tok & 7)) << 4) + ((lane & 1) << 3);
-    const uint2 v = lds64(sx + off);
-    const uint32_t b[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
-    unsigned emax = 0, emin = 255;
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const unsigned mag = b[i] & 0x7fffu;
-        const unsigned e = mag >> 7;
-        emax = e > emax ? e : emax;
-        const unsigned ez = mag ? e : 255u;      // exact zeros do not bound the range
-        emin = ez < emin ? ez : emin;
-        bad |= (e == 255u);
-    }
-    emax = warp_max_u32(emax);
-    emin = warp_min_u32(emin);
-    const bool ok = !__any_sync(0xffffffffu, bad) &&
-                    (emax == 0u || (emax >= 15u && emin + 31u >= emax));
-    const float f = (ok && emax) ? __uint_as_float((268u - emax) << 23) : 0.f;
-    const float x0 = __uint_as_float(v.x << 16) * f, x1 = __uint_as_float(v.x & 0xffff0000u) * f;
-    const float x2 = __uint_as_float(v.y << 16) * f, x3 = __uint_as_float(v.y & 0xffff0000u) * f;
-    sts64(sxh + off, f32x2_to_f16x2(x0, x1), f32x2_to_f16x2(x2, x3));
-    if (lane == 0) *unscale = emax ? __uint_as_float((emax - 14u) << 23) : 1.f;
-    return ok;
-}
-
-// Bounded barrier among the 8 consumer warps (lane 0 of each warp arrives on
-// an mbarrier of count 8; every lane waits for the phase).  False if the wait
-// gave up.
-__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, int lane,
-                                           unsigned* err) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(bar));
-    const bool ok = mbar_wait_bounded(smem_u32(bar), phase, err, kErrGroupWait);
-    phase ^= 1u;
-    return ok;
-}
-
 // ------------------------------------------------------------------ fix-up
 
 // Last arriver of a split tile: y[m][n0 + rr] = sum of the tile's partial
-// slots in segment order (+ bias, one rounding); every slot is zeroed after
-// it is read.  Only the first contributing segment can have started in an
-// earlier tile (its slot 1); every later one started in this tile (slot 0),
-// so their slots lie at a fixed stride and 16 loads are kept in flight.
+// slots in segment order (+ bias, one rounding).  Every contributing slot was
+// written in this call before its ticket was taken.  Only the first
+// contributing segment can have started in an earlier tile (its slot 1); every
+// later one started in this tile (slot 0), so their slots lie at a fixed
+// stride and 16 loads are kept in flight.
 template <int MTB>
 __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int j_first, int j_last,
                                            int tid) {
@@ -561,10 +566,8 @@ __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int 
     const int sl_first = (seg_begin(p, j_first) / p.KB == tile) ? 0 : 1;
     for (int idx = tid; idx < p.M * kBN; idx += kConsumerThreads) {
         const int m = idx / kBN, rr = idx % kBN;
-        float* first = p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN + m * kBN + rr;
-        float v = ld_cg_f32(first);
-        st_cg_f32(first, 0.f);
-        float* base = p.partials + (long long)m * kBN + rr;
+        float v = ld_cg_f32(p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN + m * kBN + rr);
+        const float* base = p.partials + (long long)m * kBN + rr;
         for (int j0 = j_first + 1; j0 <= j_last; j0 += kBatch) {
             float val[kBatch];
 #pragma unroll
@@ -573,11 +576,6 @@ __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int 
 #pragma unroll
             for (int q = 0; q < kBatch; ++q)
                 if (j0 + q <= j_last) v += val[q];       // ascending segment order
-            // Leave the workspace all-zero: a later call with another shape may
-            // place its arrival tickets over these bytes.
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q)
-                if (j0 + q <= j_last) st_cg_f32(base + (long long)(j0 + q) * kStride, 0.f);
         }
         if (n0 + rr < p.N) write_output(p, m, n0 + rr, v);
     }
@@ -593,8 +591,6 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     constexpr int MTB = XRows<MT>::v;
     constexpr int W_BYTES = TileBytes<DT>::w;
     constexpr int X_BYTES = MTB * kBK * 2;
-    constexpr bool kHalfX = (DT == kFP8 && FAM == kMMA);
-    constexpr int kLoaderWarp = kConsumerWarps;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -603,19 +599,13 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const SmemLayout L = smem_layout(DT, FAM, MT, S);
     uint8_t* sW = smem + L.w;
     uint8_t* sX = smem + L.x;
-    uint8_t* sXh = smem + L.xh;                                          // [S][X_BYTES]
     StageHeader* hdr = reinterpret_cast<StageHeader*>(smem + L.hdr);
-    float* unscale = reinterpret_cast<float*>(smem + L.unscale);       // [S][16]
-    uint8_t* bad = smem + L.bad;                                        // [S][16]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + S;
-    uint64_t* xready = empty + S;
-    uint64_t* gbar = xready + S;
-    // flag[0..1]: the tile to finish at a run end, double-buffered by the group
-    // barrier's phase so that thread 0 never overwrites a value a slower warp
-    // has yet to read; flag[2]: abort.
-    volatile int* flag = reinterpret_cast<volatile int*>(smem + L.flags);
-    volatile int* abort_flag = flag + 2;
+    uint64_t* written = empty + S;    // [2] consumer warps -> ticket warp (count 8)
+    uint64_t* result = written + 2;   // [2] ticket warp -> consumer warps (count 1)
+    volatile RunSlot* runs = reinterpret_cast<volatile RunSlot*>(smem + L.runs);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.runs + 2 * sizeof(RunSlot));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
@@ -626,10 +616,11 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), kConsumerWarps);
-            mbar_init(smem_u32(&xready[s]), kConsumerWarps);
         }
-        mbar_init(smem_u32(gbar), kConsumerWarps);
-        flag[0] = flag[1] = -1;
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&written[b]), kConsumerWarps);
+            mbar_init(smem_u32(&result[b]), 1);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
         griddep_launch_dependents();
@@ -642,6 +633,29 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // Everyone but the loader sleeps until the previous kernel on the stream
     // has finished (a hardware wait, no polling while it runs).
     if (warp != kLoaderWarp) griddep_wait();
+
+    // ---------------------------------------------------------------- ticket warp
+    // For each split run, in order: wait until all consumer warps have stored
+    // their partial rows, take the tile's ticket (acquire-release at GPU scope:
+    // publishes those rows, and for the last arriver makes every other
+    // contributor's rows visible), publish the outcome.
+    if (warp == kTicketWarp) {
+        if (lane == 0) {
+            uint32_t wph = 0u;        // phase parity of written[b] in bit b
+            for (int r = 0;; ++r) {
+                const int b = r & 1;
+                if (!mbar_wait_bounded(smem_u32(&written[b]), (wph >> b) & 1u, err, kErrRunWait))
+                    break;
+                wph ^= 1u << b;
+                const int tile = runs[b].tile;
+                if (tile < 0) break;
+                const int old = atom_add_acq_rel_gpu(&p.tickets[tile], 1);
+                runs[b].last = (old == runs[b].jl - runs[b].jf) ? tile : -1;
+                mbar_arrive(smem_u32(&result[b]));
+            }
+        }
+        return;
+    }
 
     // ---------------------------------------------------------------- loader
     if (warp == kLoaderWarp) {
@@ -657,14 +671,25 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 if constexpr (DT == kBF16)
                     tma_load_2d(dw + kBN * 128, &tm_w, bar, kb * kBK + 64, tile * kBN, pol_w);
             };
+            // x of the unit (FP8: the f16 copy, and its unscale factors into the
+            // header; both written by the prep kernel, so only after the wait).
             auto issue_x = [&](int s, int kb) {
                 const uint32_t bar = smem_u32(&full[s]);
+                if constexpr (DT == kFP8) {
+                    const float* us = p.unscale + (long long)kb * kUnscaleStride;
+#pragma unroll
+                    for (int q = 0; q < MTB / 4; ++q)
+                        cp_async_16(smem_u32(&hdr[s].unscale[4 * q]), us + 4 * q);
+                    cp_async_mbar_arrive(bar);
+                }
                 const uint32_t dx = smem_u32(sX + (size_t)s * X_BYTES);
                 tma_load_2d(dx, &tm_x, bar, kb * kBK, 0, pol_x);
                 tma_load_2d(dx + MTB * 128, &tm_x, bar, kb * kBK + 64, 0, pol_x);
             };
-            // Header + scale + arrival for unit (tile, kb); `left` = units left in
-            // the segment including this one.  No division on this path.
+            // Header + block scale + arrival for unit (tile, kb); `left` = units
+            // left in the segment including this one.  No division on this path.
+            // The expected bytes include the x copies issued later, so the stage
+            // cannot complete before they (and the cp.asyncs before them) land.
             auto open_stage = [&](int s, int tile, int kb, int seg, bool seg_first, long long left) {
                 int fl = 0;
                 if (seg_first || kb == 0) fl |= kRunFirst;
@@ -674,8 +699,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 hdr[s].seg = seg;
                 hdr[s].flags = fl;
                 const uint32_t bar = smem_u32(&full[s]);
-                if constexpr (DT == kFP8)
-                    cp_async_4_mbar(smem_u32(&hdr[s].scale), p.scales + (long long)tile * KB + kb, bar);
+                if constexpr (DT == kFP8) {
+                    cp_async_4(smem_u32(&hdr[s].scale), p.scales + (long long)tile * KB + kb);
+                    cp_async_mbar_arrive(bar);
+                }
                 mbar_arrive_expect_tx(bar, W_BYTES + X_BYTES);
             };
 
@@ -683,9 +710,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             long long u0 = seg_begin(p, seg);
             long long u1 = seg_begin(p, seg + 1);
             int tile = (int)(u0 / KB), kb = (int)(u0 % KB);
-            // Weights and scales never change between the layers of one stream:
-            // prefetch the first stages' weight tiles before waiting for the
-            // previous kernel; everything else waits.
+            // Weights and scales are never written by the previous kernel when
+            // early_weights is set: prefetch the first stages' weight tiles
+            // before waiting for it; everything else waits.
             long long pre = 0;
             if (p.early_weights) {
                 pre = u1 - u0 < S ? u1 - u0 : S;
@@ -702,24 +729,28 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 if (++kb == KB) { kb = 0; ++tile; }
             }
             issued = pre;
+            // Stage and ring pass of unit `issued`, kept incrementally (the stage
+            // count is a run-time value: no division on this path).
+            int ls = (int)pre;
+            uint32_t lph = 0;
+            if (ls == S) { ls = 0; lph = 1; }
             long long left = u1 - u0 - pre;
             bool seg_first = pre == 0;
             while (ok) {
                 for (; left > 0; --left) {
-                    const int s = (int)(issued % S);
-                    const uint32_t ph = (uint32_t)((issued / S) & 1);
                     if (issued >= S &&
-                        !mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, err, kErrProducerWait)) {
+                        !mbar_wait_bounded(smem_u32(&empty[ls]), lph ^ 1u, err, kErrProducerWait)) {
                         ok = false;
                         *abort_flag = 1;
                         break;
                     }
-                    open_stage(s, tile, kb, seg, seg_first, left);
-                    issue_w(s, tile, kb);
-                    issue_x(s, kb);
+                    open_stage(ls, tile, kb, seg, seg_first, left);
+                    issue_w(ls, tile, kb);
+                    issue_x(ls, kb);
                     seg_first = false;
                     if (++kb == KB) { kb = 0; ++tile; }
                     ++issued;
+                    if (++ls == S) { ls = 0; lph ^= 1u; }
                 }
                 if (!ok) break;
                 // Claim the next segment after the first wave; the unsigned range
@@ -736,12 +767,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             }
             // Tell the consumers there is no more work.
             {
-                const int s = (int)(issued % S);
-                const uint32_t ph = (uint32_t)((issued / S) & 1);
                 if (issued < S ||
-                    mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, err, kErrProducerWait)) {
-                    hdr[s].flags = kDone;
-                    mbar_arrive(smem_u32(&full[s]));
+                    mbar_wait_bounded(smem_u32(&empty[ls]), lph ^ 1u, err, kErrProducerWait)) {
+                    hdr[ls].flags = kDone;
+                    mbar_arrive(smem_u32(&full[ls]));
                     ++issued;
                 } else {
                     *abort_flag = 1;
@@ -769,99 +798,55 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // ---------------------------------------------------------------- consumers
     Consumer c;
     c.reset();
-    uint32_t gphase = 0;
     int run_kb0 = 0;
-    // Deferred ticket of the last split run (thread 0 only).
-    int pend_old = -1, pend_tile = -1, pend_jf = 0, pend_jl = 0;
+    int n_split = 0;                  // split runs handed to the ticket warp so far
+    uint32_t rph = 0u;                // phase parity of result[b] in bit b
 
-    // Thread 0 publishes whether the pending split tile is complete; after the
-    // barrier every consumer helps finish it.
-    auto settle_pending = [&]() -> bool {
-        const int fb = (int)(gphase & 1u);
-        if (threadIdx.x == 0)
-            flag[fb] = (pend_tile >= 0 && pend_old == pend_jl - pend_jf) ? pend_tile : -1;
-        if (!group_sync(gbar, gphase, lane, err)) return false;
-        const int ft = flag[fb];
+    // Hand split run `tile` (partial rows already stored) to the ticket warp;
+    // tile < 0 tells it that there are no more.
+    auto hand_over = [&](int tile, int jf, int jl) {
+        const int b = n_split & 1;
+        if (threadIdx.x == 0) {
+            runs[b].tile = tile;
+            runs[b].jf = jf;
+            runs[b].jl = jl;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&written[b]));
+    };
+    // Outcome of split run q: if it completed its tile, every consumer thread
+    // helps finish the tile.  False if the wait gave up.
+    auto settle = [&](int q) -> bool {
+        const int b = q & 1;
+        if (!mbar_wait_bounded(smem_u32(&result[b]), (rph >> b) & 1u, err, kErrRunWait))
+            return false;
+        rph ^= 1u << b;
+        const int ft = runs[b].last;
         if (ft >= 0) {
             const long long tu0 = (long long)ft * KB;
             fixup_tile<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + KB - 1), threadIdx.x);
-        }
-        if (threadIdx.x == 0) {
-            if (ft >= 0) p.tickets[ft] = 0;
-            pend_tile = -1;
+            if (threadIdx.x == 0) p.tickets[ft] = 0;
         }
         return true;
     };
 
-    // FP8 MMA: consumer warp w rescales x of token(s) w (and w + 8) of a stage.
-    auto prepare_stage = [&](int s) {
-        if constexpr (kHalfX) {
-            const uint32_t sx = smem_u32(sX + (size_t)s * X_BYTES);
-            const uint32_t sxh = smem_u32(sXh + (size_t)s * X_BYTES);
-#pragma unroll
-            for (int tok = warp; tok < MTB; tok += kConsumerWarps) {
-                bool okx = true;
-                if (tok < p.M) okx = scale_token_to_f16<MTB>(sx, sxh, tok, lane, unscale + s * 16 + tok);
-                if (lane == 0) bad[s * 16 + tok] = okx ? 0 : 1;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&xready[s]));
-        }
-    };
-
-    bool alive = true;
-    if constexpr (kHalfX) {
-        // Prologue: prepare stage 0.
-        if (!mbar_wait_bounded(smem_u32(&full[0]), 0, err, kErrConsumerWait)) {
+    // Stage s and ring-pass parity ph of the unit being consumed, kept
+    // incrementally (no division by the run-time stage count).
+    int s = 0;
+    uint32_t ph = 0;
+    while (true) {
+        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, err, kErrConsumerWait)) {
             *abort_flag = 1;
-            alive = false;
-        } else if (!(hdr[0].flags & kDone)) {
-            prepare_stage(0);
+            break;
         }
-    }
-    for (long long i = 0; alive; ++i) {
-        const int s = (int)(i % S);
-        const uint32_t ph = (uint32_t)((i / S) & 1);
-        if constexpr (!kHalfX) {
-            if (!mbar_wait_bounded(smem_u32(&full[s]), ph, err, kErrConsumerWait)) {
-                *abort_flag = 1;
-                break;
-            }
-        }
-        if (*abort_flag) break;
-        const int flags = hdr[s].flags;
-        if (flags & kDone) break;
-        const int tile = hdr[s].tile, kb = hdr[s].kb;
-        const int seg = hdr[s].seg;
+        const StageHeader& hd = hdr[s];
+        const int flags = hd.flags;
+        if ((flags & kDone) || *abort_flag) break;
+        const int tile = hd.tile, kb = hd.kb;
+        const int seg = hd.seg;
         if (flags & kRunFirst) run_kb0 = kb;
-
-        uint32_t sxh = 0;
-        const float* uns = nullptr;
-        bool exact_bf16 = false;
-        if constexpr (kHalfX) {
-            // Look one stage ahead: rescale this warp's token of the next stage
-            // while the other warps finish this stage's.
-            const long long i1 = i + 1;
-            const int s1 = (int)(i1 % S);
-            if (!mbar_wait_bounded(smem_u32(&full[s1]), (uint32_t)((i1 / S) & 1), err,
-                                   kErrConsumerWait)) {
-                *abort_flag = 1;
-                break;
-            }
-            if (!(hdr[s1].flags & kDone)) prepare_stage(s1);
-            if (!mbar_wait_bounded(smem_u32(&xready[s]), ph, err, kErrConsumerWait)) {
-                *abort_flag = 1;
-                break;
-            }
-            sxh = smem_u32(sXh + (size_t)s * X_BYTES);
-            uns = unscale + s * 16;
-            const uint4 bv = *reinterpret_cast<const uint4*>(bad + s * 16);
-            exact_bf16 = ((MTB > 8 ? (bv.z | bv.w) : 0u) | bv.x | bv.y) != 0u;
-        }
-        float scale = 1.f;
-        if constexpr (DT == kFP8) scale = hdr[s].scale;
-        c.consume(smem_u32(sW + (size_t)s * W_BYTES), smem_u32(sX + (size_t)s * X_BYTES), sxh, uns,
-                  exact_bf16, warp, lane, scale);
+        c.consume(smem_u32(sW + (size_t)s * W_BYTES), smem_u32(sX + (size_t)s * X_BYTES), hd, p,
+                  warp, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
 
@@ -875,20 +860,27 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             }
             c.write_rows(p, slot, tile * kBN, warp, lane);
             c.reset();
-            // Settle the previous split run's ticket (its atomic has had a whole
-            // run to complete), then take this one's.
-            if (!settle_pending()) { *abort_flag = 1; break; }
-            if (!whole && threadIdx.x == 0) {
-                const long long tu0 = (long long)tile * KB;
-                pend_tile = tile;
-                pend_jf = seg_of(p, tu0);
-                pend_jl = seg_of(p, tu0 + KB - 1);
-                pend_old = atom_add_acq_rel_gpu(&p.tickets[tile], 1);
+            if (!whole) {
+                // Hand this run over, then settle the previous split run (its
+                // ticket has had a whole run to come back).
+                int jf = 0, jl = 0;
+                if (threadIdx.x == 0) {
+                    const long long tu0 = (long long)tile * KB;
+                    jf = seg_of(p, tu0);
+                    jl = seg_of(p, tu0 + KB - 1);
+                }
+                hand_over(tile, jf, jl);
+                ++n_split;
+                if (n_split >= 2 && !settle(n_split - 2)) { *abort_flag = 1; break; }
             }
         }
+        if (++s == S) { s = 0; ph ^= 1u; }
     }
-    // Settle the last pending ticket before leaving.
-    if (!*abort_flag) settle_pending();
+    // Release the ticket warp and settle the last split run before leaving.
+    if (!*abort_flag) {
+        hand_over(-1, 0, 0);
+        if (n_split >= 1) settle(n_split - 1);
+    }
 }
 
 }  // namespace dl
