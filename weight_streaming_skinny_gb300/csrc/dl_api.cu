@@ -225,7 +225,7 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     pl.xh_off = pl.unscale_off = 0;
     if (dtype == DL_FP8_B128) {
         pl.xh_off = align_up(end, 256);
-        pl.unscale_off = align_up(pl.xh_off + (size_t)M * K * 2, 256);
+        pl.unscale_off = align_up(pl.xh_off + (size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256);
         end = pl.unscale_off + (size_t)pl.KB * dl::kUnscaleStride * sizeof(float);
     }
     pl.ws_bytes = end;
@@ -279,13 +279,20 @@ dl_status encode_maps(const Plan& pl, int M, int N, int K, const void* x, const 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return fail(DL_ERR_CUDA, "weight tensor map: CUresult %d", (int)r);
-    {
+    if (pl.dtype == DL_BF16) {
         const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
         const cuuint32_t box[2] = {64, (cuuint32_t)pl.mtb};
-        r = enc(&tx,
-                pl.dtype == DL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                2, const_cast<void*>(x), dims, strides, box,
+        r = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
+                ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        // The prep kernel's f16 copy: rows of 64 values, [K block][half][mtb];
+        // one box = the 4 mtb rows of two consecutive K blocks.
+        const cuuint64_t dims[2] = {64, (cuuint64_t)pl.KB * 2 * pl.mtb};
+        const cuuint64_t strides[1] = {128};
+        const cuuint32_t box[2] = {64, (cuuint32_t)(4 * pl.mtb)};
+        r = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box,
                 ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
@@ -369,7 +376,8 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
         // weights or scales, so main may always prefetch weights early.
         e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, false);
         if (e == cudaSuccess)
-            e = dl::launch_prep_x(static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, stream);
+            e = dl::launch_prep_x(static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, pl.mtb,
+                                  stream);
         if (e == cudaSuccess) {
             p.early_weights = 1;
             e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);

@@ -122,6 +122,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) global -> this CTA's shared memory, counted as transaction bytes
+// on the barrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // Asynchronous global -> shared copies (4 or 16 bytes, both addresses aligned
 // to the size) and the barrier arrival that tracks them: the barrier's pending
 // count is raised at once and lowered when every earlier cp.async of this
@@ -151,6 +162,11 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 v;
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
     return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, int a, int b, int c, int d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {

@@ -125,21 +125,27 @@ struct LinearParams {
     unsigned* err;            // device error word (bounded waits OR their bit in)
 };
 
+// One pipeline stage holds one unit, or for FP8 up to two consecutive units
+// of one run (the same 32 KB of weights as a bf16 unit).
+constexpr int kMaxUnitsPerStage = 2;
+
 struct StageHeader {
-    int tile;                 // unit held by the stage: weight rows 128*tile..
-    int kb;                   //   and K block kb
-    int seg;                  // segment it belongs to
+    int tile;                 // units held by the stage: weight rows 128*tile..,
+    int kb;                   //   K blocks kb .. kb + nkb - 1
+    int seg;                  // segment they belong to
     int flags;                // kRunFirst | kRunLast | kDone
-    float scale;              // FP8 block scale of the unit (copied asynchronously)
-    int pad[3];
-    float unscale[kUnscaleStride];   // FP8: per-token unscale factors of the k-block
+    int nkb;                  // units in the stage (1, or 2 for FP8)
+    float scale[kMaxUnitsPerStage];  // FP8 block scales (copied asynchronously)
+    int pad;
+    float unscale[kMaxUnitsPerStage][kUnscaleStride];   // FP8: per-token unscale factors
 };
-static_assert(sizeof(StageHeader) == 96, "stage header layout");
+static_assert(sizeof(StageHeader) == 160, "stage header layout");
 
 template <int DT>
 struct TileBytes {
-    static constexpr int w = kBN * kBK * (DT == kBF16 ? 2 : 1);
+    static constexpr int w = kBN * kBK * (DT == kBF16 ? 2 : 1);   // one unit
 };
+constexpr int kStageWBytes = 2 * kBN * kBK;   // weights of one stage (either dtype)
 
 template <int MT>
 struct XRows {
@@ -162,8 +168,8 @@ struct RunSlot {
 
 __host__ __device__ constexpr SmemLayout smem_layout(int dtype, int, int mt, int stages) {
     const int mtb = mt < 8 ? 8 : mt;
-    const int wbytes = kBN * kBK * (dtype == kBF16 ? 2 : 1);
-    const int xbytes = mtb * kBK * 2;
+    const int wbytes = kStageWBytes;
+    const int xbytes = mtb * kBK * 2 * (dtype == kBF16 ? 1 : kMaxUnitsPerStage);
     SmemLayout L{};
     L.w = 0;
     L.x = L.w + stages * wbytes;
@@ -234,10 +240,12 @@ struct SimtConsumer {
         for (int m = 0; m < MT; ++m) acc[0][m] = acc[1][m] = 0.f;
     }
 
-    // sw: weight tile of the stage; sx: activations of the stage (bf16, or for
-    // FP8 the exact f16 copy); hd: the stage header.
-    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, const StageHeader& hd,
-                                            const LinearParams& p, int warp, int lane) {
+    // sw: weight tile of the unit; sx: its activations (bf16, or for FP8 the
+    // exact f16 copy); FP8: its block scale, the per-token unscale factors and
+    // its K block.
+    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, float scale,
+                                            const float* unscale, int kb, const LinearParams& p,
+                                            int warp, int lane) {
         const int row = warp * 16 + (lane & 15);
         const int h = lane >> 4;
         const int sw8 = row & 7;
@@ -263,20 +271,20 @@ struct SimtConsumer {
             bool exact = true;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                u[m] = hd.unscale[m];
+                u[m] = unscale[m];
                 exact &= (u[m] != 0.f);      // token slots >= M carry 1
             }
             float part[2][MT];
             if (exact) {
                 fp8_unit_f16(sw, xbase, row, h, sw8, part);
             } else {
-                fp8_unit_exact(sw, p, hd.kb, row, h, sw8, part);
+                fp8_unit_exact(sw, p, kb, row, h, sw8, part);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) u[m] = 1.f;
             }
 #pragma unroll
             for (int m = 0; m < MT; ++m)
-                acc[0][m] = fmaf((part[0][m] + part[1][m]) * u[m], hd.scale, acc[0][m]);
+                acc[0][m] = fmaf((part[0][m] + part[1][m]) * u[m], scale, acc[0][m]);
         }
     }
 
@@ -385,8 +393,9 @@ struct MmaConsumer {
                 for (int i = 0; i < 4; ++i) acc[k][nt][i] = 0.f;
     }
 
-    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, const StageHeader& hd,
-                                            const LinearParams& p, int warp, int lane) {
+    __device__ __forceinline__ void consume(uint32_t sw, uint32_t sx, float scale,
+                                            const float* unscale, int kb, const LinearParams& p,
+                                            int warp, int lane) {
         const int mat = lane >> 3, rr = lane & 7;
         const int arow = warp * 16 + rr + ((mat & 1) << 3);
         const int aswz = arow & 7;
@@ -428,19 +437,18 @@ struct MmaConsumer {
             bool exact = true;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                u0[nt] = hd.unscale[8 * nt + 2 * t];
-                u1[nt] = hd.unscale[8 * nt + 2 * t + 1];
+                u0[nt] = unscale[8 * nt + 2 * t];
+                u1[nt] = unscale[8 * nt + 2 * t + 1];
                 exact &= (u0[nt] != 0.f) && (u1[nt] != 0.f);   // token slots >= M carry 1
             }
             float part[2][NT][4];
             if (__all_sync(0xffffffffu, exact)) {
                 fp8_unit_f16(abase, aswz, mat, sx, lane, part);
             } else {
-                fp8_unit_exact(abase, aswz, mat, p, hd.kb, lane, part);
+                fp8_unit_exact(abase, aswz, mat, p, kb, lane, part);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) u0[nt] = u1[nt] = 1.f;
             }
-            const float scale = hd.scale;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 acc[0][nt][0] = fmaf((part[0][nt][0] + part[1][nt][0]) * u0[nt], scale, acc[0][nt][0]);
@@ -589,8 +597,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
               const LinearParams p) {
     using Consumer = typename ConsumerOf<DT, FAM, MT>::type;
     constexpr int MTB = XRows<MT>::v;
-    constexpr int W_BYTES = TileBytes<DT>::w;
-    constexpr int X_BYTES = MTB * kBK * 2;
+    constexpr int W_UNIT = TileBytes<DT>::w;                 // weights of one unit
+    constexpr int X_UNIT = MTB * kBK * 2;                   // activations of one unit
+    constexpr int X_STAGE = DT == kBF16 ? X_UNIT : kMaxUnitsPerStage * X_UNIT;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -662,93 +671,116 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            long long issued = 0;
+            long long issued = 0;     // stages issued
             bool ok = true;
-            auto issue_w = [&](int s, int tile, int kb) {
+            // Units in the stage that starts at K block kb with `left` units
+            // left in the segment: FP8 pairs two K blocks of the same tile.
+            auto units_at = [&](int kb, long long left) -> int {
+                if constexpr (DT == kFP8) return (left >= 2 && kb + 1 < KB) ? 2 : 1;
+                else return 1;
+            };
+            auto issue_w = [&](int s, int tile, int kb, int nkb) {
                 const uint32_t bar = smem_u32(&full[s]);
-                const uint32_t dw = smem_u32(sW + (size_t)s * W_BYTES);
-                tma_load_2d(dw, &tm_w, bar, kb * kBK, tile * kBN, pol_w);
-                if constexpr (DT == kBF16)
+                const uint32_t dw = smem_u32(sW + (size_t)s * kStageWBytes);
+                if constexpr (DT == kBF16) {
+                    tma_load_2d(dw, &tm_w, bar, kb * kBK, tile * kBN, pol_w);
                     tma_load_2d(dw + kBN * 128, &tm_w, bar, kb * kBK + 64, tile * kBN, pol_w);
-            };
-            // x of the unit (FP8: the f16 copy, and its unscale factors into the
-            // header; both written by the prep kernel, so only after the wait).
-            auto issue_x = [&](int s, int kb) {
-                const uint32_t bar = smem_u32(&full[s]);
-                if constexpr (DT == kFP8) {
-                    const float* us = p.unscale + (long long)kb * kUnscaleStride;
-#pragma unroll
-                    for (int q = 0; q < MTB / 4; ++q)
-                        cp_async_16(smem_u32(&hdr[s].unscale[4 * q]), us + 4 * q);
-                    cp_async_mbar_arrive(bar);
+                } else {
+                    for (int u = 0; u < nkb; ++u)
+                        tma_load_2d(dw + u * W_UNIT, &tm_w, bar, (kb + u) * kBK, tile * kBN, pol_w);
                 }
-                const uint32_t dx = smem_u32(sX + (size_t)s * X_BYTES);
-                tma_load_2d(dx, &tm_x, bar, kb * kBK, 0, pol_x);
-                tma_load_2d(dx + MTB * 128, &tm_x, bar, kb * kBK + 64, 0, pol_x);
             };
-            // Header + block scale + arrival for unit (tile, kb); `left` = units
-            // left in the segment including this one.  No division on this path.
-            // The expected bytes include the x copies issued later, so the stage
-            // cannot complete before they (and the cp.asyncs before them) land.
-            auto open_stage = [&](int s, int tile, int kb, int seg, bool seg_first, long long left) {
+            // Activations of the stage.  bf16: x itself (two 64-column boxes).
+            // FP8: the prep kernel's f16 copy, laid out [K block][half][MTB][64],
+            // so one box of 4 MTB rows holds K blocks kb and kb + 1 (rows past
+            // the end read as zero), and the unscale factors by one bulk copy.
+            // Both are written by the prep kernel: only after the wait.
+            auto issue_x = [&](int s, int kb, int nkb) {
+                const uint32_t bar = smem_u32(&full[s]);
+                const uint32_t dx = smem_u32(sX + (size_t)s * X_STAGE);
+                if constexpr (DT == kFP8) {
+                    bulk_load(smem_u32(&hdr[s].unscale[0][0]), p.unscale + (long long)kb * kUnscaleStride,
+                              (uint32_t)(nkb * kUnscaleStride * 4), bar);
+                    tma_load_2d(dx, &tm_x, bar, 0, kb * 2 * MTB, pol_x);
+                } else {
+                    tma_load_2d(dx, &tm_x, bar, kb * kBK, 0, pol_x);
+                    tma_load_2d(dx + MTB * 128, &tm_x, bar, kb * kBK + 64, 0, pol_x);
+                }
+            };
+            // Header + block scales + arrival for the stage at (tile, kb) holding
+            // nkb units; `left` = units left in the segment including these.  No
+            // division on this path.  The expected bytes include the copies issued
+            // later (x, unscale), so the stage cannot complete before they land.
+            auto open_stage = [&](int s, int tile, int kb, int nkb, int seg, bool seg_first,
+                                  long long left) {
                 int fl = 0;
                 if (seg_first || kb == 0) fl |= kRunFirst;
-                if (left == 1 || kb == KB - 1) fl |= kRunLast;
-                hdr[s].tile = tile;
-                hdr[s].kb = kb;
-                hdr[s].seg = seg;
-                hdr[s].flags = fl;
+                if (left == nkb || kb + nkb == KB) fl |= kRunLast;
+                sts128(smem_u32(&hdr[s].tile), tile, kb, seg, fl);
+                hdr[s].nkb = nkb;
                 const uint32_t bar = smem_u32(&full[s]);
+                uint32_t bytes = 0;
                 if constexpr (DT == kFP8) {
-                    cp_async_4(smem_u32(&hdr[s].scale), p.scales + (long long)tile * KB + kb);
+                    for (int u = 0; u < nkb; ++u)
+                        cp_async_4(smem_u32(&hdr[s].scale[u]), p.scales + (long long)tile * KB + kb + u);
                     cp_async_mbar_arrive(bar);
+                    bytes = nkb * (W_UNIT + kUnscaleStride * 4) + X_STAGE;
+                } else {
+                    bytes = W_UNIT + X_UNIT;
                 }
-                mbar_arrive_expect_tx(bar, W_BYTES + X_BYTES);
+                mbar_arrive_expect_tx(bar, bytes);
             };
 
             int seg = blockIdx.x;
             long long u0 = seg_begin(p, seg);
             long long u1 = seg_begin(p, seg + 1);
             int tile = (int)(u0 / KB), kb = (int)(u0 % KB);
+            long long left = u1 - u0;
             // Weights and scales are never written by the previous kernel when
-            // early_weights is set: prefetch the first stages' weight tiles
-            // before waiting for it; everything else waits.
-            long long pre = 0;
+            // early_weights is set: fill the first stages' weight tiles before
+            // waiting for it; everything else waits.
+            int pre = 0;
             if (p.early_weights) {
-                pre = u1 - u0 < S ? u1 - u0 : S;
                 int ptile = tile, pkb = kb;
-                for (long long k = 0; k < pre; ++k) {
-                    open_stage((int)k, ptile, pkb, seg, k == 0, u1 - u0 - k);
-                    issue_w((int)k, ptile, pkb);
-                    if (++pkb == KB) { pkb = 0; ++ptile; }
+                long long pleft = left;
+                while (pre < S && pleft > 0) {
+                    const int nkb = units_at(pkb, pleft);
+                    open_stage(pre, ptile, pkb, nkb, seg, pre == 0, pleft);
+                    issue_w(pre, ptile, pkb, nkb);
+                    pleft -= nkb;
+                    if ((pkb += nkb) == KB) { pkb = 0; ++ptile; }
+                    ++pre;
                 }
             }
             griddep_wait();
-            for (long long k = 0; k < pre; ++k) {
-                issue_x((int)k, kb);
-                if (++kb == KB) { kb = 0; ++tile; }
+            for (int st = 0; st < pre; ++st) {
+                const int nkb = units_at(kb, left);
+                issue_x(st, kb, nkb);
+                left -= nkb;
+                if ((kb += nkb) == KB) { kb = 0; ++tile; }
             }
             issued = pre;
-            // Stage and ring pass of unit `issued`, kept incrementally (the stage
+            // Stage and ring pass of stage `issued`, kept incrementally (the stage
             // count is a run-time value: no division on this path).
-            int ls = (int)pre;
+            int ls = pre;
             uint32_t lph = 0;
             if (ls == S) { ls = 0; lph = 1; }
-            long long left = u1 - u0 - pre;
             bool seg_first = pre == 0;
             while (ok) {
-                for (; left > 0; --left) {
+                while (left > 0) {
                     if (issued >= S &&
                         !mbar_wait_bounded(smem_u32(&empty[ls]), lph ^ 1u, err, kErrProducerWait)) {
                         ok = false;
                         *abort_flag = 1;
                         break;
                     }
-                    open_stage(ls, tile, kb, seg, seg_first, left);
-                    issue_w(ls, tile, kb);
-                    issue_x(ls, kb);
+                    const int nkb = units_at(kb, left);
+                    open_stage(ls, tile, kb, nkb, seg, seg_first, left);
+                    issue_w(ls, tile, kb, nkb);
+                    issue_x(ls, kb, nkb);
                     seg_first = false;
-                    if (++kb == KB) { kb = 0; ++tile; }
+                    left -= nkb;
+                    if ((kb += nkb) == KB) { kb = 0; ++tile; }
                     ++issued;
                     if (++ls == S) { ls = 0; lph ^= 1u; }
                 }
@@ -830,7 +862,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         return true;
     };
 
-    // Stage s and ring-pass parity ph of the unit being consumed, kept
+    // Stage s and ring-pass parity ph of the stage being consumed, kept
     // incrementally (no division by the run-time stage count).
     int s = 0;
     uint32_t ph = 0;
@@ -840,19 +872,27 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             break;
         }
         const StageHeader& hd = hdr[s];
-        const int flags = hd.flags;
+        const uint4 h4 = lds128(smem_u32(&hd.tile));      // tile, kb, seg, flags
+        const int tile = (int)h4.x, kb = (int)h4.y, seg = (int)h4.z, flags = (int)h4.w;
         if ((flags & kDone) || *abort_flag) break;
-        const int tile = hd.tile, kb = hd.kb;
-        const int seg = hd.seg;
         if (flags & kRunFirst) run_kb0 = kb;
-        c.consume(smem_u32(sW + (size_t)s * W_BYTES), smem_u32(sX + (size_t)s * X_BYTES), hd, p,
-                  warp, lane);
+        const uint32_t sw = smem_u32(sW + (size_t)s * kStageWBytes);
+        const uint32_t sx = smem_u32(sX + (size_t)s * X_STAGE);
+        int nkb = 1;
+        if constexpr (DT == kFP8) {
+            nkb = hd.nkb;
+            c.consume(sw, sx, hd.scale[0], hd.unscale[0], kb, p, warp, lane);
+            if (nkb == 2)
+                c.consume(sw + W_UNIT, sx + X_UNIT, hd.scale[1], hd.unscale[1], kb + 1, p, warp, lane);
+        } else {
+            c.consume(sw, sx, 1.f, nullptr, kb, p, warp, lane);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
 
         if (flags & kRunLast) {
             // This run of `tile` is complete: store its rows (y, or the slot).
-            const bool whole = (run_kb0 == 0) && (kb == KB - 1);
+            const bool whole = (run_kb0 == 0) && (kb + nkb == KB);
             float* slot = nullptr;
             if (!whole) {
                 const long long first_tile = seg_begin(p, seg) / KB;

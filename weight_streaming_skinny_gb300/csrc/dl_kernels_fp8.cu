@@ -5,18 +5,20 @@ namespace dl {
 
 // ------------------------------------------------------------------ FP8 activation prep
 
-// x (bf16 [M][K]) -> xh (f16 [M][K]): each (token, 128-column block) is scaled
+// x (bf16 [M][K]) -> xh (f16): each (token, 128-column block) is scaled
 // by 2^(141 - e), e the largest biased exponent of the block's values, so that
 // its largest magnitude lands in [2^14, 2^15); every value is then exact in
 // f16 if no non-zero value has a biased exponent below e - 31 (f16 subnormals
 // keep 8 significant bits down to 2^-17) and none is an infinity or NaN.
 // unscale[kb][tok] = 2^(e - 141) (1 for an all-zero block and for the token
-// slots tok >= M), or 0 when the block is not exact in f16.  One warp per
-// (block, token slot); lane l handles 4 values.  K % 128 == 0.
+// slots tok >= M), or 0 when the block is not exact in f16.  xh is laid out
+// [K block][half][mtb token rows][64], rows tok >= M zero, so that the main
+// kernel fetches the activations of one or two K blocks with one tensor copy.
+// One warp per (block, token slot); lane l handles 4 values.  K % 128 == 0.
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict__ x,
                                                      uint16_t* __restrict__ xh,
                                                      float* __restrict__ unscale, int M, int K,
-                                                     int KB) {
+                                                     int KB, int mtb) {
     // x may be the previous kernel's output, and the main kernel that follows
     // prefetches weights as soon as this grid lets it launch: both wait for the
     // previous kernel first.
@@ -25,12 +27,14 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict_
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int kb = w / kUnscaleStride, tok = w % kUnscaleStride;
     if (kb >= KB) return;
+    // this lane's 4 values: half lane/16, elements (lane%16)*4 .. +3 of it
+    const long long dst = (((long long)kb * 2 + (lane >> 4)) * mtb + tok) * 64 + (lane & 15) * 4;
     if (tok >= M) {
+        if (tok < mtb) stg64(xh + dst, 0u, 0u);
         if (lane == 0) unscale[kb * kUnscaleStride + tok] = 1.f;
         return;
     }
-    const long long off = (long long)tok * K + (long long)kb * kBK + lane * 4;
-    const uint2 v = ldg64(x + off);
+    const uint2 v = ldg64(x + (long long)tok * K + (long long)kb * kBK + lane * 4);
     const uint32_t b[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
     unsigned emax = 0, emin = 255;
     bool bad = false;
@@ -50,7 +54,7 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict_
     const float f = (ok && emax) ? __uint_as_float((268u - emax) << 23) : 0.f;
     const float x0 = __uint_as_float(v.x << 16) * f, x1 = __uint_as_float(v.x & 0xffff0000u) * f;
     const float x2 = __uint_as_float(v.y << 16) * f, x3 = __uint_as_float(v.y & 0xffff0000u) * f;
-    stg64(xh + off, f32x2_to_f16x2(x0, x1), f32x2_to_f16x2(x2, x3));
+    stg64(xh + dst, f32x2_to_f16x2(x0, x1), f32x2_to_f16x2(x2, x3));
     if (lane == 0)
         unscale[kb * kUnscaleStride + tok] =
             !ok ? 0.f : (emax ? __uint_as_float((emax - 14u) << 23) : 1.f);
@@ -64,7 +68,7 @@ cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const C
 }
 
 cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M, int K, int KB,
-                          cudaStream_t stream) {
+                          int mtb, cudaStream_t stream) {
     // One warp per (k-block, token slot), 8 warps per block.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((KB * kUnscaleStride + 7) / 8));
@@ -76,7 +80,7 @@ cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prep_x_kernel, x, xh, unscale, M, K, KB);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prep_x_kernel, x, xh, unscale, M, K, KB, mtb);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -28,9 +28,10 @@ cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const C
                               const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
                               bool launch);
 
-// FP8 activation prep: x (bf16 [M][K]) -> xh (f16 [M][K], exact per-block
-// power-of-two scaling) and unscale[KB][16]; K % 128 == 0.
+// FP8 activation prep: x (bf16 [M][K]) -> xh (f16 [KB][2][mtb][64], exact
+// per-block power-of-two scaling, rows >= M zero) and unscale[KB][16];
+// K % 128 == 0.
 cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M, int K, int KB,
-                          cudaStream_t stream);
+                          int mtb, cudaStream_t stream);
 
 }  // namespace dl
