@@ -92,6 +92,12 @@ constexpr int kTicketWarp = kConsumerWarps + 1;   // warp 9: split-K arrival tic
 constexpr int kThreads = kConsumerThreads + 64;
 constexpr int kMaxWaves = 24;
 constexpr int kUnscaleStride = 16;       // unscale factors per k-block (one per token slot)
+// Stages a loader fills before it waits for the previous kernel (more delays
+// its first activation copy), and the most stages it may have in flight when
+// it claims another segment: enough to cover HBM latency at one SM's share of
+// the bandwidth, few enough that the last claims leave little backlog.
+constexpr int kEarlyStages = 3;
+constexpr int kClaimDepth = 3;
 
 enum DType { kBF16 = 0, kFP8 = 1 };
 enum Family { kSIMT = 1, kMMA = 2 };
@@ -743,7 +749,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             if (p.early_weights) {
                 int ptile = tile, pkb = kb;
                 long long pleft = left;
-                while (pre < S && pleft > 0) {
+                while (pre < S && pre < kEarlyStages && pleft > 0) {
                     const int nkb = units_at(pkb, pleft);
                     open_stage(pre, ptile, pkb, nkb, seg, pre == 0, pleft);
                     issue_w(pre, ptile, pkb, nkb);
@@ -785,6 +791,19 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     if (++ls == S) { ls = 0; lph ^= 1u; }
                 }
                 if (!ok) break;
+                // Claim only when at most kClaimDepth issued stages are still
+                // unconsumed, so that no CTA holds a long backlog when the
+                // shared segments run out: wait for stage issued - kClaimDepth
+                // to be released (its ring slot and pass follow from ls, lph).
+                if (issued >= kClaimDepth && kClaimDepth < S) {
+                    const bool wrap = ls < kClaimDepth;
+                    const int qs = wrap ? ls - kClaimDepth + S : ls - kClaimDepth;
+                    if (!mbar_wait_bounded(smem_u32(&empty[qs]), wrap ? lph ^ 1u : lph, err,
+                                           kErrProducerWait)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
                 // Claim the next segment after the first wave; the unsigned range
                 // check keeps every index in bounds even with a corrupted counter.
                 const unsigned claimed = (unsigned)atomicAdd(&p.counter[0], 1);
