@@ -295,7 +295,9 @@ struct SimtConsumer {
     }
 
     // One FP8 unit against the exact f16 copy of x: codes 16cc..16cc+15 of the
-    // row (cc = 4h + j) pair with f16 chunks 2j, 2j+1 of x box h.
+    // row (cc = 4h + j) pair with 16-column group j of x box h, stored in the
+    // fragment order of the prep kernel: its word w < 4 holds columns 4w, 4w+1
+    // and word 4 + w columns 4w + 2, 4w + 3.
     __device__ __forceinline__ void fp8_unit_f16(uint32_t sw, uint32_t xbase, int row, int h,
                                                  int sw8, float (&part)[2][MT]) {
         const uint32_t wbase = sw + row * 128;
@@ -315,13 +317,13 @@ struct SimtConsumer {
                 const uint4 x0 = lds128(xbase + m * 128 + (((2 * j) ^ (m & 7)) << 4));
                 const uint4 x1 = lds128(xbase + m * 128 + (((2 * j + 1) ^ (m & 7)) << 4));
                 float a = part[j & 1][m];
-                a = fma2_f16(wh[0], x0.x, a);
-                a = fma2_f16(wh[1], x0.y, a);
-                a = fma2_f16(wh[2], x0.z, a);
-                a = fma2_f16(wh[3], x0.w, a);
-                a = fma2_f16(wh[4], x1.x, a);
-                a = fma2_f16(wh[5], x1.y, a);
-                a = fma2_f16(wh[6], x1.z, a);
+                a = fma2_f16(wh[0], x0.x, a);     // columns 0, 1
+                a = fma2_f16(wh[1], x1.x, a);     //         2, 3
+                a = fma2_f16(wh[2], x0.y, a);     //         4, 5
+                a = fma2_f16(wh[3], x1.y, a);
+                a = fma2_f16(wh[4], x0.z, a);
+                a = fma2_f16(wh[5], x1.z, a);
+                a = fma2_f16(wh[6], x0.w, a);
                 a = fma2_f16(wh[7], x1.w, a);
                 part[j & 1][m] = a;
             }
@@ -468,11 +470,12 @@ struct MmaConsumer {
     // One FP8 unit (this warp's 16 rows x 128 codes) as an f16 MMA against the
     // exact f16 copy of x.  Step s is the 16-code chunk s of each row.  Thread
     // (g, t) receives codes 4t..4t+3 of its rows' chunk; they stand for
-    // fragment columns {2t, 2t+1} and {2t+8, 2t+9}, so its B fragment is
-    // x[token][16s + 4t .. 16s + 4t + 3], 8 bytes of the swizzled x box.
+    // fragment columns {2t, 2t+1} and {2t+8, 2t+9}, and the prep kernel stored
+    // x in that order, so the B fragments come from ldmatrix exactly as for
+    // bf16 weights (bank-conflict free on the swizzled tile).
     __device__ __forceinline__ void fp8_unit_f16(uint32_t abase, int aswz, int mat, uint32_t sx,
                                                  int lane, float (&part)[2][NT][4]) {
-        const int g = lane >> 2, t = lane & 3;
+        const int rr = lane & 7;
 #pragma unroll
         for (int k = 0; k < 2; ++k)
 #pragma unroll
@@ -483,20 +486,31 @@ struct MmaConsumer {
         for (int s = 0; s < 8; s += 2) {
             uint32_t q[4];
             ldmatrix_x4(abase + (((s + (mat >> 1)) ^ aswz) << 4), q[0], q[1], q[2], q[3]);
+            // B fragments of steps s and s + 1: chunks c0 .. c0 + 3 of box s / 4
+            const uint32_t xbox = sx + (s >> 2) * (MT * 128);
+            const int c0 = (s & 3) * 2;
+            uint32_t b[2][NT][2];
+            if constexpr (MT == 8) {
+                uint32_t r[4];
+                ldmatrix_x4(xbox + rr * 128 + (((c0 + mat) ^ rr) << 4), r[0], r[1], r[2], r[3]);
+                b[0][0][0] = r[0]; b[0][0][1] = r[1];
+                b[1][0][0] = r[2]; b[1][0][1] = r[3];
+            } else {
+                const int tok = rr + ((mat >> 1) << 3);
+                uint32_t r[4], u[4];
+                ldmatrix_x4(xbox + tok * 128 + (((c0 + (mat & 1)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
+                ldmatrix_x4(xbox + tok * 128 + (((c0 + 2 + (mat & 1)) ^ (tok & 7)) << 4), u[0], u[1], u[2], u[3]);
+                b[0][0][0] = r[0]; b[0][0][1] = r[1]; b[0][1][0] = r[2]; b[0][1][1] = r[3];
+                b[1][0][0] = u[0]; b[1][0][1] = u[1]; b[1][1][0] = u[2]; b[1][1][1] = u[3];
+            }
 #pragma unroll
             for (int ss = 0; ss < 2; ++ss) {
-                const int step = s + ss;
                 uint32_t A0, A1, A2, A3;
                 e4m3x4_to_f16x2x2(q[2 * ss], A0, A2);       // row g
                 e4m3x4_to_f16x2x2(q[2 * ss + 1], A1, A3);   // row g + 8
-                const uint32_t xbox = sx + (step >> 2) * (MT * 128);
-                const int xc = 2 * (step & 3) + (t >> 1);   // logical 16-byte chunk
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int tok = g + 8 * nt;
-                    const uint2 xb = lds64(xbox + tok * 128 + ((xc ^ (tok & 7)) << 4) + ((t & 1) << 3));
-                    mma_f16_16816(part[ss][nt], A0, A1, A2, A3, xb.x, xb.y);
-                }
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16_16816(part[ss][nt], A0, A1, A2, A3, b[ss][nt][0], b[ss][nt][1]);
             }
         }
     }

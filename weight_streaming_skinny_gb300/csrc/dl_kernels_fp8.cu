@@ -14,6 +14,11 @@ namespace dl {
 // slots tok >= M), or 0 when the block is not exact in f16.  xh is laid out
 // [K block][half][mtb token rows][64], rows tok >= M zero, so that the main
 // kernel fetches the activations of one or two K blocks with one tensor copy.
+// Within every group of 16 columns the values are stored in the order the
+// FP8 MMA fragments take them (position 2t + j holds column 4t + j and
+// position 2t + 8 + j holds column 4t + 2 + j, t < 4, j < 2): a plain
+// ldmatrix of a token row then yields the B fragment that matches the e4m3
+// codes 4t .. 4t + 3 a thread receives for the A operand.
 // One warp per (block, token slot); lane l handles 4 values.  K % 128 == 0.
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict__ x,
                                                      uint16_t* __restrict__ xh,
@@ -27,10 +32,17 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict_
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int kb = w / kUnscaleStride, tok = w % kUnscaleStride;
     if (kb >= KB) return;
-    // this lane's 4 values: half lane/16, elements (lane%16)*4 .. +3 of it
-    const long long dst = (((long long)kb * 2 + (lane >> 4)) * mtb + tok) * 64 + (lane & 15) * 4;
+    // This lane's 4 columns 4t .. 4t + 3 (t = lane % 4) of 16-column group
+    // (lane % 16) / 4 of half lane / 16 go to positions 2t, 2t + 1 and
+    // 2t + 8, 2t + 9 of that group.
+    const long long row = (((long long)kb * 2 + (lane >> 4)) * mtb + tok) * 64 + ((lane & 15) >> 2) * 16;
+    uint16_t* d0 = xh + row + 2 * (lane & 3);
+    uint16_t* d1 = d0 + 8;
     if (tok >= M) {
-        if (tok < mtb) stg64(xh + dst, 0u, 0u);
+        if (tok < mtb) {
+            *reinterpret_cast<uint32_t*>(d0) = 0u;
+            *reinterpret_cast<uint32_t*>(d1) = 0u;
+        }
         if (lane == 0) unscale[kb * kUnscaleStride + tok] = 1.f;
         return;
     }
@@ -54,7 +66,8 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict_
     const float f = (ok && emax) ? __uint_as_float((268u - emax) << 23) : 0.f;
     const float x0 = __uint_as_float(v.x << 16) * f, x1 = __uint_as_float(v.x & 0xffff0000u) * f;
     const float x2 = __uint_as_float(v.y << 16) * f, x3 = __uint_as_float(v.y & 0xffff0000u) * f;
-    stg64(xh + dst, f32x2_to_f16x2(x0, x1), f32x2_to_f16x2(x2, x3));
+    *reinterpret_cast<uint32_t*>(d0) = f32x2_to_f16x2(x0, x1);
+    *reinterpret_cast<uint32_t*>(d1) = f32x2_to_f16x2(x2, x3);
     if (lane == 0)
         unscale[kb * kUnscaleStride + tok] =
             !ok ? 0.f : (emax ? __uint_as_float((emax - 14u) << 23) : 1.f);
