@@ -213,25 +213,29 @@ def test_column_split_example_on_gpu(cuda_device, family):
 
 @pytest.mark.parametrize("family", FAMILIES)
 def test_mlp_split_example_two_way_split_k_on_gpu(cuda_device, family):
-    """Second linear of the MLP example with K split over two CTAs at hidden unit 4."""
-    dl.set_override(family, 0, 2)          # 2 K-blocks -> exactly 2 CTAs, one per block
+    """Second linear of the MLP example with K split over two CTAs at hidden unit 4.
+    A work unit is 128 columns of bf16 and 256 columns of FP8, so the second half
+    of the hidden units starts at column 128 (bf16) or 256 (FP8): two units,
+    exactly two CTAs, one per unit."""
+    dl.set_override(family, 0, 2)
     g = json.load(open(os.path.join(GOLDEN, "mlp_split_example.json")))
     x, a, b = (np.array(g[k], dtype=np.float64) for k in ("x", "a", "b"))
     h = np.maximum(x @ a, 0.0)             # small integers: exact; the example's ReLU
-    hp = np.zeros((2, 256)); hp[:, 0:4] = h[:, 0:4]; hp[:, 128:132] = h[:, 4:8]
-    wp = np.zeros((4, 256)); wp[:, 0:4] = b.T[:, 0:4]; wp[:, 128:132] = b.T[:, 4:8]
     y32 = torch.empty(2, 4, dtype=torch.float32, device=cuda_device)
     for fmt in ("bf16", "fp8"):
+        half = 128 if fmt == "bf16" else 256
+        hp = np.zeros((2, 2 * half)); hp[:, 0:4] = h[:, 0:4]; hp[:, half:half + 4] = h[:, 4:8]
+        wp = np.zeros((4, 2 * half)); wp[:, 0:4] = b.T[:, 0:4]; wp[:, half:half + 4] = b.T[:, 4:8]
         def run(xx):
             if fmt == "bf16":
                 dl.linear_bf16(_bits_tensor(xx, cuda_device), _bits_tensor(wp, cuda_device), out_f32=y32)
             else:
                 dl.linear_fp8_block128(_bits_tensor(xx, cuda_device), _codes_tensor(wp, cuda_device),
-                                       torch.ones(1, 2, device=cuda_device), out_f32=y32)
+                                       torch.ones(1, 4, device=cuda_device), out_f32=y32)
             return y32.cpu()
         assert torch.equal(run(hp), torch.tensor(g["printed_all_reduce_sum"], dtype=torch.float32))
-        h0 = hp.copy(); h0[:, 128:] = 0
-        h1 = hp.copy(); h1[:, :128] = 0
+        h0 = hp.copy(); h0[:, half:] = 0
+        h1 = hp.copy(); h1[:, :half] = 0
         assert torch.equal(run(h0), torch.tensor(g["printed_device0_partial"], dtype=torch.float32))
         assert torch.equal(run(h1), torch.tensor(g["printed_device1_partial"], dtype=torch.float32))
 

@@ -95,7 +95,7 @@ dl_status device_info(DeviceInfo& out) {
 // and the split of the units among CTAs, pipeline depth, workspace layout.
 struct Plan {
     int dtype, family, mt, mtb;
-    int KB, n_tiles;
+    int KB, UT, n_tiles;
     long long units;
     int grid;
     int n_segments;
@@ -149,7 +149,10 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     pl.n_tiles = (N + dl::kBN - 1) / dl::kBN;
     if (pl.n_tiles > kMaxTiles)
         return fail(DL_ERR_UNSUPPORTED_SHAPE, "N=%d exceeds %d rows", N, kMaxTiles * dl::kBN);
-    pl.units = (long long)pl.n_tiles * pl.KB;
+    // Partition units of 32 KB of weights: one 128-column K block of bf16, two
+    // of FP8 (the last one single when KB is odd).
+    pl.UT = dtype == DL_BF16 ? pl.KB : (pl.KB + 1) / 2;
+    pl.units = (long long)pl.n_tiles * pl.UT;
     // Grid: persistent, `cps` CTAs per SM: by default one, with all of the
     // SM's shared memory; the override ctas_per_sm = 2 sizes the grid for two,
     // each with half of it.
@@ -174,8 +177,8 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     {
         const long long G = pl.grid, U = pl.units;
         long long min_seg = 2;
-        const long long by_tile = (pl.KB + 23) / 24;
-        const long long by_m = dtype == DL_BF16 ? (M + 3) / 4 : (M + 1) / 2;
+        const long long by_tile = (pl.UT + 23) / 24;
+        const long long by_m = (M + 3) / 4;
         if (by_tile > min_seg) min_seg = by_tile;
         if (by_m > min_seg) min_seg = by_m;
         long long s0 = (U * 5 / 8) / G;
@@ -353,6 +356,7 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.N = N;
     p.K = K;
     p.KB = pl.KB;
+    p.UT = pl.UT;
     p.n_tiles = pl.n_tiles;
     p.units = pl.units;
     p.n_segments = pl.n_segments;

@@ -1,8 +1,9 @@
 // The decode-linear kernel: y[M,N] = x[M,K] . w[N,K]^T (+ bias), M <= 16.
 //
 // Work decomposition.  The weight matrix is cut into tiles of kBN = 128 rows;
-// each tile's K range is cut into units of kBK = 128 columns (one FP8 scale
-// block).  The U = tiles x k-blocks units, in tile-major order, are cut into
+// each tile's K range is cut into units of 32 KB of weights: 128 columns of
+// bf16, or 256 columns (two 128x128 scale blocks) of FP8.  The U = tiles x
+// units-per-tile units, in tile-major order, are cut into
 // contiguous segments by a partition fixed by (M, N, K, SM count) alone: a
 // first wave of one large segment per CTA (about 5/8 of the work), then waves
 // of segments that halve in size down to a small minimum.  A persistent grid
@@ -118,9 +119,11 @@ struct LinearParams {
     int* tickets;             // [n_tiles] arrival counters (zero between calls)
     float* partials;          // [n_segments][2][MTB][kBN] fp32 (scratch)
     int M, N, K;
-    int KB;                   // k-blocks per tile = ceil(K / 128)
+    int KB;                   // 128-column K blocks per tile = ceil(K / 128)
+    int UT;                   // partition units per tile: bf16 one K block each (UT = KB),
+                              //   FP8 two (UT = ceil(KB / 2), the last one single if KB is odd)
     int n_tiles;
-    long long units;          // n_tiles * KB
+    long long units;          // n_tiles * UT
     int n_segments;
     int n_waves;              // the partition: wave w holds segments
     int wave_seg0[kMaxWaves + 1];     //   [wave_seg0[w], wave_seg0[w+1]), each of
@@ -591,7 +594,7 @@ __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int 
     constexpr int kBatch = 16;
     constexpr long long kStride = 2LL * MTB * kBN;            // floats between segments' slot 0
     const int n0 = tile * kBN;
-    const int sl_first = (seg_begin(p, j_first) / p.KB == tile) ? 0 : 1;
+    const int sl_first = (seg_begin(p, j_first) / p.UT == tile) ? 0 : 1;
     for (int idx = tid; idx < p.M * kBN; idx += kConsumerThreads) {
         const int m = idx / kBN, rr = idx % kBN;
         float v = ld_cg_f32(p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN + m * kBN + rr);
@@ -639,6 +642,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
     const int KB = p.KB;
+    const int UT = p.UT;
+    constexpr int kUnitKB = DT == kBF16 ? 1 : kMaxUnitsPerStage;   // K blocks per unit
     unsigned* err = p.err;
 
     if (threadIdx.x == 0) {
@@ -693,10 +698,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             const uint64_t pol_x = policy_evict_last();
             long long issued = 0;     // stages issued
             bool ok = true;
-            // Units in the stage that starts at K block kb with `left` units
-            // left in the segment: FP8 pairs two K blocks of the same tile.
-            auto units_at = [&](int kb, long long left) -> int {
-                if constexpr (DT == kFP8) return (left >= 2 && kb + 1 < KB) ? 2 : 1;
+            // K blocks of unit ku of a tile: kb = ku * kUnitKB, and one or two.
+            auto blocks_of = [&](int ku) -> int {
+                if constexpr (DT == kFP8) return ku * 2 + 1 < KB ? 2 : 1;
                 else return 1;
             };
             auto issue_w = [&](int s, int tile, int kb, int nkb) {
@@ -727,15 +731,16 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     tma_load_2d(dx + MTB * 128, &tm_x, bar, kb * kBK + 64, 0, pol_x);
                 }
             };
-            // Header + block scales + arrival for the stage at (tile, kb) holding
-            // nkb units; `left` = units left in the segment including these.  No
-            // division on this path.  The expected bytes include the copies issued
-            // later (x, unscale), so the stage cannot complete before they land.
-            auto open_stage = [&](int s, int tile, int kb, int nkb, int seg, bool seg_first,
-                                  long long left) {
+            // Header + block scales + arrival for unit (tile, ku): K blocks kb ..
+            // kb + nkb - 1; `left` = units left in the segment including this one.
+            // No division on this path.  The expected bytes include the copies
+            // issued later (x, unscale), so the stage cannot complete before they
+            // land.
+            auto open_stage = [&](int s, int tile, int ku, int seg, bool seg_first, long long left) {
+                const int kb = ku * kUnitKB, nkb = blocks_of(ku);
                 int fl = 0;
-                if (seg_first || kb == 0) fl |= kRunFirst;
-                if (left == nkb || kb + nkb == KB) fl |= kRunLast;
+                if (seg_first || ku == 0) fl |= kRunFirst;
+                if (left == 1 || ku == UT - 1) fl |= kRunLast;
                 sts128(smem_u32(&hdr[s].tile), tile, kb, seg, fl);
                 hdr[s].nkb = nkb;
                 const uint32_t bar = smem_u32(&full[s]);
@@ -754,31 +759,26 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             int seg = blockIdx.x;
             long long u0 = seg_begin(p, seg);
             long long u1 = seg_begin(p, seg + 1);
-            int tile = (int)(u0 / KB), kb = (int)(u0 % KB);
+            int tile = (int)(u0 / UT), ku = (int)(u0 % UT);
             long long left = u1 - u0;
             // Weights and scales are never written by the previous kernel when
             // early_weights is set: fill the first stages' weight tiles before
             // waiting for it; everything else waits.
             int pre = 0;
             if (p.early_weights) {
-                int ptile = tile, pkb = kb;
-                long long pleft = left;
-                while (pre < S && pre < kEarlyStages && pleft > 0) {
-                    const int nkb = units_at(pkb, pleft);
-                    open_stage(pre, ptile, pkb, nkb, seg, pre == 0, pleft);
-                    issue_w(pre, ptile, pkb, nkb);
-                    pleft -= nkb;
-                    if ((pkb += nkb) == KB) { pkb = 0; ++ptile; }
-                    ++pre;
+                int ptile = tile, pku = ku;
+                for (; pre < S && pre < kEarlyStages && pre < left; ++pre) {
+                    open_stage(pre, ptile, pku, seg, pre == 0, left - pre);
+                    issue_w(pre, ptile, pku * kUnitKB, blocks_of(pku));
+                    if (++pku == UT) { pku = 0; ++ptile; }
                 }
             }
             griddep_wait();
             for (int st = 0; st < pre; ++st) {
-                const int nkb = units_at(kb, left);
-                issue_x(st, kb, nkb);
-                left -= nkb;
-                if ((kb += nkb) == KB) { kb = 0; ++tile; }
+                issue_x(st, ku * kUnitKB, blocks_of(ku));
+                if (++ku == UT) { ku = 0; ++tile; }
             }
+            left -= pre;
             issued = pre;
             // Stage and ring pass of stage `issued`, kept incrementally (the stage
             // count is a run-time value: no division on this path).
@@ -787,20 +787,18 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             if (ls == S) { ls = 0; lph = 1; }
             bool seg_first = pre == 0;
             while (ok) {
-                while (left > 0) {
+                for (; left > 0; --left) {
                     if (issued >= S &&
                         !mbar_wait_bounded(smem_u32(&empty[ls]), lph ^ 1u, err, kErrProducerWait)) {
                         ok = false;
                         *abort_flag = 1;
                         break;
                     }
-                    const int nkb = units_at(kb, left);
-                    open_stage(ls, tile, kb, nkb, seg, seg_first, left);
-                    issue_w(ls, tile, kb, nkb);
-                    issue_x(ls, kb, nkb);
+                    open_stage(ls, tile, ku, seg, seg_first, left);
+                    issue_w(ls, tile, ku * kUnitKB, blocks_of(ku));
+                    issue_x(ls, ku * kUnitKB, blocks_of(ku));
                     seg_first = false;
-                    left -= nkb;
-                    if ((kb += nkb) == KB) { kb = 0; ++tile; }
+                    if (++ku == UT) { ku = 0; ++tile; }
                     ++issued;
                     if (++ls == S) { ls = 0; lph ^= 1u; }
                 }
@@ -825,8 +823,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 seg = G + (int)claimed;
                 u0 = seg_begin(p, seg);
                 u1 = seg_begin(p, seg + 1);
-                tile = (int)(u0 / KB);
-                kb = (int)(u0 % KB);
+                tile = (int)(u0 / UT);
+                ku = (int)(u0 % UT);
                 left = u1 - u0;
                 seg_first = true;
             }
@@ -888,8 +886,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         rph ^= 1u << b;
         const int ft = runs[b].last;
         if (ft >= 0) {
-            const long long tu0 = (long long)ft * KB;
-            fixup_tile<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + KB - 1), threadIdx.x);
+            const long long tu0 = (long long)ft * UT;
+            fixup_tile<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + UT - 1), threadIdx.x);
             if (threadIdx.x == 0) p.tickets[ft] = 0;
         }
         return true;
@@ -928,7 +926,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             const bool whole = (run_kb0 == 0) && (kb + nkb == KB);
             float* slot = nullptr;
             if (!whole) {
-                const long long first_tile = seg_begin(p, seg) / KB;
+                const long long first_tile = seg_begin(p, seg) / UT;
                 slot = p.partials + ((long long)seg * 2 + (tile == first_tile ? 0 : 1)) * MTB * kBN;
             }
             c.write_rows(p, slot, tile * kBN, warp, lane);
@@ -938,9 +936,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 // ticket has had a whole run to come back).
                 int jf = 0, jl = 0;
                 if (threadIdx.x == 0) {
-                    const long long tu0 = (long long)tile * KB;
+                    const long long tu0 = (long long)tile * UT;
                     jf = seg_of(p, tu0);
-                    jl = seg_of(p, tu0 + KB - 1);
+                    jl = seg_of(p, tu0 + UT - 1);
                 }
                 hand_over(tile, jf, jl);
                 ++n_split;
