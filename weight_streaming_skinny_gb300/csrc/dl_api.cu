@@ -49,6 +49,9 @@ std::atomic<int> g_cps_override{0};
 std::atomic<int> g_max_ctas_override{0};
 
 constexpr int kMaxStages = 16;
+// Stages whose weights a single FP8 call's main kernel fetches while the prep
+// kernel runs (more delays its first activation copy).
+constexpr int kEarlyStagesAfterPrep = 3;
 constexpr int kMaxDevices = 64;
 // Workspace prefix that must be zero before a call (and is zero after it):
 // the claim/done counters, then one arrival ticket per tile.  Fixed in size,
@@ -325,7 +328,10 @@ dl_status validate(int dtype, int M, int N, int K, const void* x, const void* W,
 dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void* W,
                        const float* scales, const void* bias, void* y, float* y_f32,
                        void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di,
-                       bool early_weights) {
+                       bool after_own) {
+    // after_own: every earlier kernel on the stream is one of this library's
+    // (a later layer of one dl_decode_stream call), so none writes weights or
+    // scales and the next one's weights may be fetched before the wait.
     Plan pl;
     dl_status s = make_plan(dtype, M, N, K, di, pl);
     if (s != DL_OK) return s;
@@ -368,24 +374,26 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     }
     p.wave_seg0[dl::kMaxWaves] = pl.wave_seg0[pl.n_waves];
     p.stages = pl.stages;
-    p.early_weights = early_weights ? 1 : 0;
     p.err = di.err_word;
     cudaError_t e;
     if (dtype == DL_BF16) {
+        // Inside a stream the previous layer's tail is long: fill the whole ring.
+        p.early_stages = after_own ? pl.stages : 0;
         e = dl::launch_linear_bf16(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
     } else {
         // The main kernel's attribute first (the only host-side step that can
-        // fail for it), then prep -> main.  The prep kernel lets main launch
-        // only after its own predecessor has completed and never writes
-        // weights or scales, so main may always prefetch weights early.
+        // fail for it), then prep -> main.  The prep kernel never writes
+        // weights or scales.  Alone, it lets main launch only after its own
+        // predecessor has completed, and main then prefetches a few stages
+        // during the short prep; inside a stream it lets main launch at once,
+        // so main fills its whole ring during the previous layer's tail.
+        p.early_stages = after_own ? pl.stages : kEarlyStagesAfterPrep;
         e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, false);
         if (e == cudaSuccess)
             e = dl::launch_prep_x(static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, pl.mtb,
-                                  stream);
-        if (e == cudaSuccess) {
-            p.early_weights = 1;
+                                  after_own, stream);
+        if (e == cudaSuccess)
             e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
-        }
     }
     if (e != cudaSuccess) return fail(DL_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return DL_OK;

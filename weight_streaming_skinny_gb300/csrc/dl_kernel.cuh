@@ -70,11 +70,11 @@
 // soon as it starts (griddepcontrol.launch_dependents); all its threads but
 // the loader sleep in griddepcontrol.wait until the previous kernel has
 // finished, and the loader touches nothing that kernel may have written before
-// that wait -- except, when `early_weights` is set (the previous kernel is
-// known never to write weights or scales: this kernel for an earlier layer of
-// one dl_decode_stream call, or the activation prep kernel, which itself
-// waits for its predecessor before it lets this one launch), the weight tiles
-// and scales of its first stages, which it prefetches meanwhile.
+// that wait -- except, when `early_stages` is set (the kernels before it are
+// known never to write weights or scales: earlier layers of one
+// dl_decode_stream call, or for a single FP8 call the activation prep kernel,
+// which waits for its own predecessor before it lets this one launch), the
+// weight tiles and scales of its first stages, which it prefetches meanwhile.
 //
 // Every wait is bounded (mbarrier waits give up after ~2 s, set a bit of the
 // device error word and make the CTA leave in an orderly way).
@@ -93,11 +93,9 @@ constexpr int kTicketWarp = kConsumerWarps + 1;   // warp 9: split-K arrival tic
 constexpr int kThreads = kConsumerThreads + 64;
 constexpr int kMaxWaves = 24;
 constexpr int kUnscaleStride = 16;       // unscale factors per k-block (one per token slot)
-// Stages a loader fills before it waits for the previous kernel (more delays
-// its first activation copy), and the most stages it may have in flight when
-// it claims another segment: enough to cover HBM latency at one SM's share of
-// the bandwidth, few enough that the last claims leave little backlog.
-constexpr int kEarlyStages = 3;
+// The most stages a loader may have in flight when it claims another segment:
+// enough to cover HBM latency at one SM's share of the bandwidth, few enough
+// that the last claims leave little backlog.
 constexpr int kClaimDepth = 3;
 
 enum DType { kBF16 = 0, kFP8 = 1 };
@@ -130,7 +128,8 @@ struct LinearParams {
     long long wave_unit0[kMaxWaves];  //   wave_size[w] units from wave_unit0[w]
     int wave_size[kMaxWaves];         //   (the very last segment ends at U)
     int stages;
-    int early_weights;        // prefetch the first weight tiles before griddepcontrol.wait
+    int early_stages;         // stages whose weights may be fetched before griddepcontrol.wait
+                              //   (0: the previous kernel may write weights)
     unsigned* err;            // device error word (bounded waits OR their bit in)
 };
 
@@ -762,12 +761,13 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             int tile = (int)(u0 / UT), ku = (int)(u0 % UT);
             long long left = u1 - u0;
             // Weights and scales are never written by the previous kernel when
-            // early_weights is set: fill the first stages' weight tiles before
-            // waiting for it; everything else waits.
+            // early_stages is set: fill that many stages' weight tiles before
+            // waiting for it (more delays the first activation copy when the
+            // previous kernel is short); everything else waits.
             int pre = 0;
-            if (p.early_weights) {
+            if (p.early_stages > 0) {
                 int ptile = tile, pku = ku;
-                for (; pre < S && pre < kEarlyStages && pre < left; ++pre) {
+                for (; pre < S && pre < p.early_stages && pre < left; ++pre) {
                     open_stage(pre, ptile, pku, seg, pre == 0, left - pre);
                     issue_w(pre, ptile, pku * kUnitKB, blocks_of(pku));
                     if (++pku == UT) { pku = 0; ++ptile; }

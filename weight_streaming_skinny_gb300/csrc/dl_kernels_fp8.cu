@@ -23,12 +23,14 @@ namespace dl {
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict__ x,
                                                      uint16_t* __restrict__ xh,
                                                      float* __restrict__ unscale, int M, int K,
-                                                     int KB, int mtb) {
-    // x may be the previous kernel's output, and the main kernel that follows
-    // prefetches weights as soon as this grid lets it launch: both wait for the
-    // previous kernel first.
+                                                     int KB, int mtb, int early_trigger) {
+    // x may be the previous kernel's output: wait for it.  The main kernel that
+    // follows prefetches weights as soon as this grid lets it launch, so unless
+    // every kernel before is known never to write weights (early_trigger, inside
+    // one decode stream) it is let launch only after that wait.
+    if (early_trigger) griddep_launch_dependents();
     griddep_wait();
-    griddep_launch_dependents();
+    if (!early_trigger) griddep_launch_dependents();
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int kb = w / kUnscaleStride, tok = w % kUnscaleStride;
     if (kb >= KB) return;
@@ -81,7 +83,7 @@ cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const C
 }
 
 cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M, int K, int KB,
-                          int mtb, cudaStream_t stream) {
+                          int mtb, bool early_trigger, cudaStream_t stream) {
     // One warp per (k-block, token slot), 8 warps per block.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((KB * kUnscaleStride + 7) / 8));
@@ -93,7 +95,8 @@ cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prep_x_kernel, x, xh, unscale, M, K, KB, mtb);
+    cudaError_t e =
+        cudaLaunchKernelEx(&cfg, prep_x_kernel, x, xh, unscale, M, K, KB, mtb, early_trigger ? 1 : 0);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

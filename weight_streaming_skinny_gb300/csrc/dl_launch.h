@@ -31,7 +31,9 @@ cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const C
 // FP8 activation prep: x (bf16 [M][K]) -> xh (f16 [KB][2][mtb][64], exact
 // per-block power-of-two scaling, rows >= M zero) and unscale[KB][16];
 // K % 128 == 0.
+// early_trigger: let the main kernel launch before this one's wait (only when
+// no kernel before it on the stream writes weights or scales).
 cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M, int K, int KB,
-                          int mtb, cudaStream_t stream);
+                          int mtb, bool early_trigger, cudaStream_t stream);
 
 }  // namespace dl
