@@ -4,16 +4,18 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The library never does: it has no CPU
 fallback, and this oracle shares no code with it.
 
-The arithmetic lives in ``dl_oracle.c`` (plain C, IEEE double, k ascending,
-explicit E4M3FN table); this module only compiles it with the host C compiler
-and marshals numpy arrays to it.  See the C file's header for the definition
-and the passages of the pages each part follows.
+The arithmetic of the linear layer lives in ``dl_oracle.c`` (plain C, IEEE
+double, k ascending, explicit E4M3FN table); this module compiles it with the
+host C compiler and marshals numpy arrays to it.  See the C file's header for
+the definition and the passages of the pages each part follows.  The SwiGLU
+epilogue (``silu``, ``swiglu``) is written here in float64 numpy on top of it.
 
 Parity pins: e4m3 table (closed form, anchors, an independent decoder),
 bf16 decode (all 65536 patterns), one-hot columns, scale = 1 blocks,
 linearity, exact-rational brute force and the worked examples of
-"Multi-GPU Inference and Serving at Scale" (Examples 2 and 3); see
-``tests/test_oracle.py``.
+"Multi-GPU Inference and Serving at Scale" (Examples 2 and 3); SiLU closed
+forms (sigma(ln 3) = 3/4), its odd-part identity and the gate/up pairing of
+SwiGLU; see ``tests/test_oracle.py``.
 """
 from __future__ import annotations
 
@@ -148,3 +150,39 @@ def linear(dtype: int, x_bits, w, scales=None, bias_bits=None, *, rows=None,
         raise ValueError("oracle rejected its arguments")
     return (y, a) if with_abs else y
 
+
+def silu(g):
+    """SiLU in float64: silu(g) = g * sigma(g) = g / (1 + e^-g).  e^-g overflows
+    to inf for very negative g, which gives the correct limit -0."""
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def swiglu_rows(I: int):
+    """Gate and up row indices of outputs 0..I-1 in the interleaved weight
+    layout of the SwiGLU call: gate row 16 (j // 8) + j % 8, up row 8 further."""
+    j = np.arange(I, dtype=np.int64)
+    g = 16 * (j // 8) + j % 8
+    return g, g + 8
+
+
+def swiglu(dtype: int, x_bits, w, scales=None, bias_bits=None, *, outputs=None,
+           threads: int | None = None):
+    """SwiGLU reference for the interleaved gate_up weights w [N, K] (N % 16 == 0):
+    y[m][j] = silu(g) * u, g and u the reference sums (+ bias) of the gate and up
+    rows of output j ("Multi-GPU Inference and Serving at Scale", Example 3: the
+    nonlinearity between the MLP's two matrices; SwiGLU being the variant real
+    models use, in its usual SiLU-gated form).  Returns y, g, u, A_g, A_u as
+    float64 [M, n_outputs] (A = sum_k |x w| of each row, the tolerance scale).
+    outputs -- optional list of output columns j (default: all N / 2)."""
+    N = np.asarray(w).shape[0]
+    if N % 16:
+        raise ValueError("SwiGLU weights need N % 16 == 0")
+    gate, up = swiglu_rows(N // 2)
+    if outputs is not None:
+        sel = np.asarray(outputs, dtype=np.int64)
+        gate, up = gate[sel], up[sel]
+    g, ag = linear(dtype, x_bits, w, scales, bias_bits, rows=gate, threads=threads)
+    u, au = linear(dtype, x_bits, w, scales, bias_bits, rows=up, threads=threads)
+    return silu(g) * u, g, u, ag, au

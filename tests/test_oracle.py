@@ -302,3 +302,61 @@ def test_rejects_bad_arguments():
         oracle.linear(oracle.BF16, xb, np.zeros((2, 64), dtype=np.uint16))       # K mismatch
     with pytest.raises(ValueError):
         oracle.linear(oracle.BF16, xb, np.zeros((2, 128), dtype=np.uint16), rows=[2])
+
+
+# ------------------------------------------------------------------ SwiGLU epilogue
+
+def test_silu_closed_forms():
+    """sigma(ln 3) = 3/4 and sigma(-ln 3) = 1/4 exactly; silu(0) = 0; far from 0,
+    silu(x) -> x (x > 0) and -> 0 from below (x < 0)."""
+    ln3 = math.log(3.0)
+    got = oracle.silu(np.array([ln3, -ln3, 0.0, 64.0, -64.0, -800.0]))
+    assert got[0] == pytest.approx(0.75 * ln3, rel=1e-15)
+    assert got[1] == pytest.approx(-0.25 * ln3, rel=1e-15)
+    assert got[2] == 0.0
+    assert got[3] == 64.0                       # sigma(64) rounds to 1 in double
+    assert -1e-25 < got[4] < 0.0                # -64 e^-64 / (1 + e^-64)
+    assert got[5] == 0.0 and math.copysign(1.0, got[5]) < 0   # e^800 overflows: -0
+
+
+def test_silu_odd_part_identity():
+    """silu(x) - silu(-x) = x (sigma(x) + sigma(-x) = 1): catches a sign slip."""
+    x = np.linspace(-30.0, 30.0, 241)
+    assert np.allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=1e-14, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP8_B128])
+def test_swiglu_pairs_gate_and_up_rows(dtype):
+    """x = e_0 selects column 0: g_j and u_j are exactly the values placed in
+    the gate and up rows of output j; gates alternate 0 (silu = 0) and 64
+    (silu = 64 exactly), ups are distinct integers, so y_j is 0 or 64 u_j and a
+    swapped or shifted pairing shows."""
+    I, K = 24, 128
+    gate_vals = np.where(np.arange(I) % 2 == 0, 0.0, 64.0)
+    # 24 distinct values exact in both bf16 and e4m3
+    up_vals = np.array([1, 1.5, 2, 2.5, 3, 3.5, 4, 5, 6, 7, 8, 10, 12, 14, 16, 20, 24, 28, 32, 40,
+                        48, 56, 64, 80], dtype=np.float64) * np.where(np.arange(I) % 3 == 0, -1, 1)
+    gate_rows, up_rows = oracle.swiglu_rows(I)
+    W = np.zeros((2 * I, K))
+    W[gate_rows, 0] = gate_vals
+    W[up_rows, 0] = up_vals
+    x = np.zeros((1, K)); x[0, 0] = 1.0
+    xb = _bf16_bits_of(x)
+    if dtype == oracle.BF16:
+        y, g, u, _, _ = oracle.swiglu(dtype, xb, _bf16_bits_of(W))
+    else:
+        y, g, u, _, _ = oracle.swiglu(dtype, xb, _e4m3_code_of(W), np.ones((1, 1), np.float32))
+    assert np.array_equal(g[0], gate_vals) and np.array_equal(u[0], up_vals)
+    assert np.array_equal(y[0], np.where(gate_vals == 64.0, 64.0 * up_vals, 0.0))
+
+
+def test_swiglu_rows_match_the_binding_layout():
+    """The oracle's pairing is the layout interleave_gate_up produces."""
+    import torch
+    import weight_streaming_skinny_gb300 as dl
+    I = 40
+    gate = torch.arange(I, dtype=torch.float64)[:, None]
+    up = -1.0 - gate
+    w = dl.interleave_gate_up(gate, up)[:, 0].numpy()
+    gr, ur = oracle.swiglu_rows(I)
+    assert np.array_equal(w[gr], gate[:, 0].numpy()) and np.array_equal(w[ur], up[:, 0].numpy())
