@@ -147,46 +147,56 @@ WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8
 
 
 def layer_specs(workload: str):
-    """[(dtype, M, N, K, bias, name)], config id."""
+    """[(dtype, M, N, K, bias, name, act)], config id.  act = 1: gate_up with the
+    fused SwiGLU epilogue (y holds N/2 columns)."""
     from weight_streaming_skinny_gb300 import inputs
     shapes = inputs.QWEN72B_SHAPES
     if workload == "qwen72b_layer_bf16_m1":
-        return [(inputs.DTYPE_BF16, 1, *shapes[n][:2], shapes[n][2], n) for n in shapes], 1
+        return [(inputs.DTYPE_BF16, 1, *shapes[n][:2], shapes[n][2], n, 0) for n in shapes], 1
     if workload == "qwen72b_layer_fp8_m6":
-        return [(inputs.DTYPE_FP8_B128, 6, *shapes[n][:2], shapes[n][2], n) for n in shapes], 2
+        return [(inputs.DTYPE_FP8_B128, 6, *shapes[n][:2], shapes[n][2], n, 0) for n in shapes], 2
     if workload == "qwen72b_model_fp8_m1":
         specs = []
         for layer in range(inputs.QWEN72B_LAYERS):
             for n in shapes:
-                specs.append((inputs.DTYPE_FP8_B128, 1, *shapes[n][:2], shapes[n][2], f"{n}.{layer}"))
+                specs.append((inputs.DTYPE_FP8_B128, 1, *shapes[n][:2], shapes[n][2], f"{n}.{layer}",
+                              1 if n == "gate_up" else 0))
         N, K, b = inputs.QWEN72B_LM_HEAD
-        specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head"))
+        specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 0))
         return specs, 4
     raise ValueError(workload)
 
 
+def out_cols(L) -> int:
+    """Columns of a layer's y (N, or N/2 with the SwiGLU epilogue)."""
+    return L.N // 2 if getattr(L, "act", 0) else L.N
+
+
 def build_layers(workload, dev):
-    """Seeded layers on `dev`.  In the whole-model stream, a layer reads the
-    previous layer's output when the shapes chain (down -> next QKV, O ->
-    gate_up); attention and the MLP activation are not part of this path, so O
-    and down read fixed activation buffers."""
-    import torch
+    """Seeded layers on `dev` (each LayerInputs gets an `act` attribute).  In the
+    whole-model stream a layer reads the previous layer's output where the
+    model does: down -> next QKV, O -> gate_up, gate_up (SwiGLU) -> down, last
+    down -> lm_head.  Attention is not part of this path, so O reads a fixed
+    activation buffer."""
     from weight_streaming_skinny_gb300 import inputs
     specs, cfg = layer_specs(workload)
     out = []
-    for i, (dt, M, N, K, bias, name) in enumerate(specs):
+    for i, (dt, M, N, K, bias, name, act) in enumerate(specs):
         L = inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg, layer_idx=i, device=dev)
+        L.act = act
         out.append((name, L))
     if workload == "qwen72b_model_fp8_m1":
         for i in range(1, len(out)):
             prev, cur = out[i - 1][1], out[i][1]
-            if prev.N == cur.K and prev.M == cur.M and out[i][0].split(".")[0] in ("qkv", "gate_up", "lm_head"):
+            if out_cols(prev) == cur.K and prev.M == cur.M and out[i][0].split(".")[0] != "o":
                 cur.x = None          # chained: filled with the previous layer's y below
     return out
 
 
 def launch(dl, L, y, ws, stream):
-    if L.dtype == "bf16":
+    if getattr(L, "act", 0):
+        dl.linear_swiglu(L.x, L.w, L.scales, L.bias, out=y, workspace=ws, stream=stream)
+    elif L.dtype == "bf16":
         dl.linear_bf16(L.x, L.w, L.bias, out=y, workspace=ws, stream=stream)
     else:
         dl.linear_fp8_block128(L.x, L.w, L.scales, L.bias, out=y, workspace=ws, stream=stream)
@@ -204,17 +214,20 @@ def run_ours(args, rank, world, dist):
     dl.set_override({"auto": 0, "simt": 1, "mma": 2}[args.kernel], 0, 0)
     workload = args.workload
     layers = build_layers(workload, dev)
-    ys = [torch.empty((L.M, L.N), dtype=torch.bfloat16, device=dev) for _, L in layers]
+    ys = [torch.empty((L.M, out_cols(L)), dtype=torch.bfloat16, device=dev) for _, L in layers]
     for j in range(1, len(layers)):
         if layers[j][1].x is None:
             layers[j][1].x = ys[j - 1]
     ws = dl.Workspace.for_shapes(
         [(L.M, L.N, L.K, dl.BF16 if L.dtype == "bf16" else dl.FP8_B128) for _, L in layers], dev)
     stream = torch.cuda.Stream(dev)
-    nbytes = [L.algorithmic_bytes for _, L in layers]
+    # algorithmic bytes; a SwiGLU layer writes M x N/2 outputs instead of M x N
+    nbytes = [L.algorithmic_bytes - (L.M * L.N if L.act else 0) for _, L in layers]
     step_bytes = sum(nbytes)
     dl_layers = [dl.Layer(dl.BF16 if L.dtype == "bf16" else dl.FP8_B128, L.x, L.w, ys[j],
-                          L.scales, L.bias) for j, (_, L) in enumerate(layers)]
+                          L.scales, L.bias, act=L.act) for j, (_, L) in enumerate(layers)]
+    # kernels per step: one per layer, two for FP8 (activation prep + main)
+    launches_per_step = sum(1 if L.dtype == "bf16" else 2 for _, L in layers)
     use_graph = args.mode == "graph"
     torch.cuda.synchronize(dev)
 
@@ -295,7 +308,7 @@ def run_ours(args, rank, world, dist):
         chained_in = [j > 0 and layers[j][1].x is ys[j - 1] for j in range(len(layers))]
         chained_out = [j + 1 < len(layers) and chained_in[j + 1] for j in range(len(layers))]
         hx = [L.x.cpu().pin_memory() for _, L in layers]
-        hy = [torch.empty((L.M, L.N), dtype=torch.bfloat16).pin_memory() for _, L in layers]
+        hy = [torch.empty((L.M, out_cols(L)), dtype=torch.bfloat16).pin_memory() for _, L in layers]
         h2d = sum(x.numel() * 2 for j, x in enumerate(hx) if not chained_in[j])
         d2h = sum(y.numel() * 2 for j, y in enumerate(hy) if not chained_out[j])
         E = max(3, min(K, 50))
@@ -348,8 +361,15 @@ def run_ours(args, rank, world, dist):
         "ms_per_token": round(ms_per_step, 4),
         "ceiling_ms_at_measured_peak": round(step_bytes / (peak * 1e9) * 1e3, 4),
         "clock_window": f"timed region + {extra_steps} untimed steps of the same workload",
-        "gpu_launches": len(layers) * K, "step_bytes": step_bytes,
+        "gpu_launches": launches_per_step * K, "step_bytes": step_bytes,
     }, layers
+
+
+def _host_copy(L):
+    """LayerInputs on the host, keeping the `act` attribute."""
+    H = L.to("cpu")
+    H.act = getattr(L, "act", 0)
+    return H
 
 
 def cpu_oracle_gbs(layers_host, budget_s: float, row_frac: float = 1.0):
@@ -360,24 +380,32 @@ def cpu_oracle_gbs(layers_host, budget_s: float, row_frac: float = 1.0):
     from weight_streaming_skinny_gb300 import inputs
     prepared = []
     for name, L in layers_host:
-        n = max(1, int(L.N * row_frac))
-        rows = np.linspace(0, L.N - 1, n).astype(np.int64)
+        act = getattr(L, "act", 0)
+        ncols = L.N // 2 if act else L.N
+        n = max(1, int(ncols * row_frac))                 # outputs computed
+        cols = np.linspace(0, ncols - 1, n).astype(np.int64)
+        nw = 2 * n if act else n                          # weight rows read
         xb = inputs.bf16_bits(L.x)
         bb = None if L.bias is None else inputs.bf16_bits(L.bias)
         if L.dtype == "bf16":
             args = (oracle.BF16, xb, inputs.bf16_bits(L.w), None, bb)
-            wbytes = 2 * n * L.K
+            wbytes = 2 * nw * L.K
         else:
             args = (oracle.FP8_B128, xb, inputs.u8_codes(L.w), L.scales.cpu().numpy(), bb)
-            wbytes = n * L.K + 4 * ((n + 127) // 128) * (L.K // 128)
-        prepared.append((args, rows, wbytes + 2 * L.M * L.K + 2 * L.M * n + (2 * n if bb is not None else 0)))
+            wbytes = nw * L.K + 4 * ((nw + 127) // 128) * (L.K // 128)
+        prepared.append((args, cols, act,
+                         wbytes + 2 * L.M * L.K + 2 * L.M * n + (2 * nw if bb is not None else 0)))
     threads = oracle.default_threads()
     passes, t_total, b_total = 0, 0.0, 0
     while passes == 0 or t_total < budget_s:
-        for args, rows, b in prepared:
+        for args, cols, act, b in prepared:
             a = time.perf_counter()
-            oracle.linear(*args[:3], scales=args[3], bias_bits=args[4], rows=rows, with_abs=False,
-                          threads=threads)
+            if act:
+                oracle.swiglu(*args[:3], scales=args[3], bias_bits=args[4], outputs=cols,
+                              threads=threads)
+            else:
+                oracle.linear(*args[:3], scales=args[3], bias_bits=args[4], rows=cols,
+                              with_abs=False, threads=threads)
             t_total += time.perf_counter() - a
             b_total += b
         passes += 1
@@ -421,8 +449,11 @@ def main():
               "mode": args.mode}
     if len(specs) > 8:
         config["layers"] = {"count": len(specs), "decoder_layers": len(specs) // 4,
-                            "per_layer": [s[5].split(".")[0] for s in specs[:4]],
-                            "dtype": specs[0][0], "M": specs[0][1], "lm_head": "bf16 152064x8192"}
+                            "per_layer": [s[5].split(".")[0] + ("+swiglu" if s[6] else "")
+                                          for s in specs[:4]],
+                            "dtype": specs[0][0], "M": specs[0][1], "lm_head": "bf16 152064x8192",
+                            "chaining": "down -> next qkv, o -> gate_up, gate_up (SwiGLU) -> down, "
+                                        "last down -> lm_head"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -434,9 +465,10 @@ def main():
             specs_all, cfg = layer_specs(args.workload)
             layers = []
             for i in (0, 1, 2, 3, len(specs_all) - 1):
-                dt, M, N, K, bias, name = specs_all[i]
-                layers.append((name, inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg,
-                                                       layer_idx=i, device="cpu")))
+                dt, M, N, K, bias, name, act = specs_all[i]
+                Lh = inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg, layer_idx=i, device="cpu")
+                Lh.act = act
+                layers.append((name, Lh))
         else:
             layers = build_layers(args.workload, "cpu")
         sample_frac = 0.25
@@ -467,11 +499,11 @@ def main():
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
         if len(layers) > 8:
             pick = [0, 1, 2, 3, len(layers) - 1]
-            host_layers = [(layers[i][0], layers[i][1].to("cpu")) for i in pick]
+            host_layers = [(layers[i][0], _host_copy(layers[i][1])) for i in pick]
             what = ("decoder layer 0 (QKV, O, gate_up, down) and the lm_head, all rows; GB/s "
                     "applies to the whole 80-layer stream by extrapolation")
         else:
-            host_layers = [(n, L.to("cpu")) for n, L in layers]
+            host_layers = [(n, _host_copy(L)) for n, L in layers]
             what = "the whole step (all rows of the four linears)"
         v, threads, passes, t = cpu_oracle_gbs(host_layers, args.cpu_budget_s, 1.0)
         cpu = {"value": round(v, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",

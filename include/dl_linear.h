@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define DL_VERSION 1
+#define DL_VERSION 2
 
 /* Leading workspace bytes that must be zero before a call (see conventions). */
 #define DL_WORKSPACE_ZERO_BYTES (256u + 16384u * 4u)
@@ -166,6 +166,28 @@ dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* sca
 dl_status dl_linear_bf16_static_scratch(const void* x, const void* W, const void* bias, void* y,
                                         float* y_f32, int M, int N, int K, void* stream);
 
+/*
+ * gate_up projection with the SwiGLU activation fused into its epilogue:
+ *     y[m][j] = silu(g) * u,   silu(g) = g / (1 + e^-g),
+ * g and u the full fp32 sums (+ bias) of the gate and up rows of output j,
+ * evaluated in fp32 and rounded once to bf16.  This is the nonlinearity
+ * between the two matrices of the MLP in "Multi-GPU Inference and Serving at
+ * Scale", Example 3 (shown there as a ReLU; the page names SwiGLU as the
+ * variant real models use), in its usual SiLU-gated form.
+ *   dtype  DL_BF16 or DL_FP8_B128 (as for the plain calls; FP8 scales cover
+ *          128x128 blocks of W as stored)
+ *   W      [N][K] with gate and up rows interleaved in groups of 16: rows
+ *          16b .. 16b+7 are the gate rows and rows 16b+8 .. 16b+15 the up rows
+ *          of outputs 8b .. 8b+7.  N % 16 == 0 (else DL_ERR_UNSUPPORTED_SHAPE).
+ *   bias   bf16 [N] in the same row order, or NULL
+ *   y      bf16 [M][N/2]; y_f32 fp32 [M][N/2] or NULL (the value before rounding)
+ *   everything else as for dl_linear_bf16 / dl_linear_fp8_block128, with the
+ *   same workspace (dl_workspace_bytes(M, N, K, dtype)).
+ */
+dl_status dl_linear_swiglu(int dtype, const void* x, const void* W, const float* scales,
+                           const void* bias, void* y, float* y_f32, int M, int N, int K,
+                           void* workspace, size_t ws_bytes, void* stream);
+
 /* One layer of a decode weight stream (see dl_decode_stream). */
 typedef struct dl_layer {
     int dtype;             /* dl_dtype                                    */
@@ -174,7 +196,8 @@ typedef struct dl_layer {
     const void* W;         /* bf16 [N][K] or e4m3 codes [N][K]            */
     const float* scales;   /* FP8 only: fp32 [ceil(N/128)][K/128]; else NULL */
     const void* bias;      /* bf16 [N] or NULL                            */
-    void* y;               /* bf16 [M][N]                                 */
+    void* y;               /* bf16 [M][N], or [M][N/2] with act = 1       */
+    int act;               /* 0: plain; 1: SwiGLU (as dl_linear_swiglu)   */
 } dl_layer;
 
 /*

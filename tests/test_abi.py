@@ -9,7 +9,7 @@ import weight_streaming_skinny_gb300 as dl
 
 EXPECTED = {"dl_workspace_bytes", "dl_linear_bf16", "dl_linear_fp8_block128", "dl_decode_stream",
             "dl_graph_cache_clear", "dl_set_override", "dl_device_status", "dl_last_error",
-            "dl_version"}
+            "dl_version", "dl_linear_swiglu", "dl_linear_bf16_static_scratch"}
 
 
 def test_library_exports_every_header_symbol():
@@ -19,7 +19,9 @@ def test_library_exports_every_header_symbol():
 
 
 def test_version():
-    assert dl.version() == 1
+    import re
+    m = re.search(r"#define\s+DL_VERSION\s+(\d+)", open(dl._HEADER).read())
+    assert m and dl.version() == int(m.group(1)) == dl.ABI_VERSION
 
 
 # fake, well-aligned device addresses: never dereferenced, validation fails first
@@ -111,7 +113,9 @@ def test_error_message_is_thread_local_and_cleared():
     assert lib.dl_last_error() != b""
     assert lib.dl_set_override(0, 0, 0) == 0
     assert lib.dl_last_error() == b""
-    assert ctypes.sizeof(dl._Layer) == 4 * 4 + 5 * 8
+    # dl_layer: 4 ints, 5 pointers, int act (+ 4 bytes of tail padding)
+    assert ctypes.sizeof(dl._Layer) == 4 * 4 + 5 * 8 + 8
+    assert dl._Layer.act.offset == 4 * 4 + 5 * 8
 
 
 def test_workspace_zero_prefix_matches_header():
@@ -119,3 +123,22 @@ def test_workspace_zero_prefix_matches_header():
     text = open(dl._HEADER).read()
     m = re.search(r"#define\s+DL_WORKSPACE_ZERO_BYTES\s+\((\d+)u\s*\+\s*(\d+)u\s*\*\s*(\d+)u\)", text)
     assert m and int(m.group(1)) + int(m.group(2)) * int(m.group(3)) == dl.WORKSPACE_ZERO_BYTES
+
+
+def test_swiglu_validation_before_any_cuda_call():
+    """Bad SwiGLU arguments fail on the host: unknown dtype, N not a multiple of 16."""
+    lib = dl.load()
+    p = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 24)
+    assert lib.dl_linear_swiglu(7, p, p, None, None, p, None, 1, 32, 128, ws, 1 << 20, None) == 1
+    assert lib.dl_linear_swiglu(0, p, p, None, None, p, None, 1, 40, 128, ws, 1 << 20, None) == 2
+    assert b"16" in lib.dl_last_error()
+
+
+def test_interleave_gate_up_layout():
+    g = torch.arange(24 * 2, dtype=torch.float32).reshape(24, 2)
+    u = -g - 1
+    w = dl.interleave_gate_up(g, u)
+    for j in range(24):
+        b, i = divmod(j, 8)
+        assert torch.equal(w[16 * b + i], g[j]) and torch.equal(w[16 * b + 8 + i], u[j])

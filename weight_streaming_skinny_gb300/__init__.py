@@ -20,6 +20,7 @@ import torch
 __all__ = [
     "BF16", "FP8_B128", "KERNEL_AUTO", "KERNEL_SIMT", "KERNEL_MMA", "DLError", "Layer",
     "library_path", "load", "version", "workspace_bytes", "Workspace", "linear_bf16",
+    "linear_swiglu", "interleave_gate_up", "ABI_VERSION",
     "linear_bf16_static_scratch", "STATIC_SCRATCH_BYTES", "WORKSPACE_ZERO_BYTES",
     "linear_fp8_block128", "decode_stream", "graph_cache_clear", "set_override",
     "device_status", "exported_symbols", "header_symbols",
@@ -50,7 +51,10 @@ class DLError(RuntimeError):
 class _Layer(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("M", ctypes.c_int), ("N", ctypes.c_int),
                 ("K", ctypes.c_int), ("x", ctypes.c_void_p), ("W", ctypes.c_void_p),
-                ("scales", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+                ("scales", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("act", ctypes.c_int)]
+
+ABI_VERSION = 2   # DL_VERSION this binding marshals for
 
 
 def library_path() -> str:
@@ -79,10 +83,15 @@ def load():
         lib.dl_decode_stream.argtypes = [ctypes.POINTER(_Layer), i, vp, sz, vp, i]
         lib.dl_decode_stream.restype = i
         lib.dl_graph_cache_clear.restype = None
+        lib.dl_linear_swiglu.argtypes = [i, vp, vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
+        lib.dl_linear_swiglu.restype = i
         lib.dl_set_override.argtypes = [i, i, i]
         lib.dl_set_override.restype = i
         lib.dl_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.dl_device_status.restype = i
+        if lib.dl_version() != ABI_VERSION:
+            raise RuntimeError(f"{_LIB_PATH} is ABI version {lib.dl_version()}, this binding "
+                               f"marshals version {ABI_VERSION}: rebuild the library")
         _lib = lib
         return lib
 
@@ -217,6 +226,50 @@ def linear_bf16(x, w, bias=None, *, out=None, out_f32=None, workspace: Workspace
     return out
 
 
+def linear_swiglu(x, w, scales=None, bias=None, *, out=None, out_f32=None,
+                  workspace: Workspace | None = None, stream=None):
+    """out[M, N/2] = silu(g) * u: gate_up projection with the SwiGLU epilogue.
+
+    w: [N, K] bf16, or e4m3 codes (uint8 / float8_e4m3fn) with fp32 `scales`,
+    its gate and up rows interleaved in groups of 16 (rows 16b..16b+7 gate,
+    16b+8..16b+15 up, of outputs 8b..8b+7); see interleave_gate_up.
+    """
+    if isinstance(w, torch.Tensor) and w.dtype == torch.float8_e4m3fn:
+        w = w.view(torch.uint8)
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    fp8 = scales is not None
+    _need(w, "w", torch.uint8 if fp8 else torch.bfloat16, dev)
+    if fp8:
+        _need(scales, "scales", torch.float32, dev)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, dev)
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("x must be [M, K] and w [N, K]")
+    M, K = x.shape
+    N = w.shape[0]
+    if N % 16:
+        raise ValueError("SwiGLU needs N % 16 == 0")
+    out = _out(out, out_f32, M, N // 2, dev)
+    dt = FP8_B128 if fp8 else BF16
+    with torch.cuda.device(dev):
+        ws = _workspace(workspace, workspace_bytes(M, N, K, dt), dev)
+        _check(load().dl_linear_swiglu(dt, _ptr(x), _ptr(w), _ptr(scales), _ptr(bias), _ptr(out),
+                                       _ptr(out_f32), M, N, K, ws.ptr, ws.nbytes, _stream(stream, dev)))
+    return out
+
+
+def interleave_gate_up(gate: torch.Tensor, up: torch.Tensor) -> torch.Tensor:
+    """[I, K] gate and up matrices (any dtype) -> the [2I, K] row order of
+    linear_swiglu: rows 16b..16b+7 = gate rows 8b..8b+7, rows 16b+8..16b+15 =
+    the matching up rows.  I % 8 == 0.  A one-time layout step for weights
+    (plain tensor indexing, not part of the decode path)."""
+    if gate.shape != up.shape or gate.shape[0] % 8:
+        raise ValueError("gate and up must have the same [I, K] shape, I % 8 == 0")
+    I, K = gate.shape
+    return torch.stack([gate.reshape(I // 8, 8, K), up.reshape(I // 8, 8, K)], dim=1).reshape(2 * I, K)
+
+
 STATIC_SCRATCH_BYTES = 16 << 20   # DL_STATIC_SCRATCH_BYTES of include/dl_linear.h
 WORKSPACE_ZERO_BYTES = 256 + 16384 * 4   # DL_WORKSPACE_ZERO_BYTES: zero before the first call
 
@@ -295,6 +348,7 @@ class Layer:
     y: torch.Tensor
     scales: torch.Tensor | None = None
     bias: torch.Tensor | None = None
+    act: int = 0          # 1: SwiGLU epilogue (see linear_swiglu); y is then [M, N/2]
 
     def shape(self):
         return (self.x.shape[0], self.w.shape[0], self.x.shape[1], self.dtype)
@@ -308,7 +362,7 @@ def _layer_struct(L: Layer) -> _Layer:
             raise ValueError(f"layer {n} must be a contiguous CUDA tensor")
     return _Layer(dt, M, N, K, L.x.data_ptr(), w.data_ptr(),
                   None if L.scales is None else L.scales.data_ptr(),
-                  None if L.bias is None else L.bias.data_ptr(), L.y.data_ptr())
+                  None if L.bias is None else L.bias.data_ptr(), L.y.data_ptr(), int(L.act))
 
 
 def decode_stream(layers, workspace: Workspace, *, use_graph: bool = False, stream=None):

@@ -328,7 +328,7 @@ dl_status validate(int dtype, int M, int N, int K, const void* x, const void* W,
 dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void* W,
                        const float* scales, const void* bias, void* y, float* y_f32,
                        void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di,
-                       bool after_own) {
+                       bool after_own, int act) {
     // after_own: every earlier kernel on the stream is one of this library's
     // (a later layer of one dl_decode_stream call), so none writes weights or
     // scales and the next one's weights may be fetched before the wait.
@@ -361,6 +361,8 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.M = M;
     p.N = N;
     p.K = K;
+    p.act = act;
+    p.ny = act ? N / 2 : N;
     p.KB = pl.KB;
     p.UT = pl.UT;
     p.n_tiles = pl.n_tiles;
@@ -478,7 +480,7 @@ dl_status dl_linear_bf16(const void* x, const void* W, const void* bias, void* y
     DeviceInfo di;
     if ((s = device_info(di)) != DL_OK) return s;
     s = launch_layer(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32, workspace, ws_bytes,
-                     static_cast<cudaStream_t>(stream), di, false);
+                     static_cast<cudaStream_t>(stream), di, false, 0);
     return s == DL_OK ? ok() : s;
 }
 
@@ -503,7 +505,7 @@ dl_status dl_linear_bf16_static_scratch(const void* x, const void* W, const void
     cudaError_t e = cudaMemsetAsync(scratch, 0, pl.tickets_off + (size_t)pl.n_tiles * sizeof(int), st);
     if (e != cudaSuccess) return fail(DL_ERR_CUDA, "clearing the static scratch: %s", cudaGetErrorString(e));
     s = launch_layer(DL_BF16, M, N, K, x, W, nullptr, bias, y, y_f32, scratch,
-                     (size_t)DL_STATIC_SCRATCH_BYTES, st, di, false);
+                     (size_t)DL_STATIC_SCRATCH_BYTES, st, di, false, 0);
     return s == DL_OK ? ok() : s;
 }
 
@@ -516,7 +518,24 @@ dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* sca
     DeviceInfo di;
     if ((s = device_info(di)) != DL_OK) return s;
     s = launch_layer(DL_FP8_B128, M, N, K, x, Wq, scales, bias, y, y_f32, workspace, ws_bytes,
-                     static_cast<cudaStream_t>(stream), di, false);
+                     static_cast<cudaStream_t>(stream), di, false, 0);
+    return s == DL_OK ? ok() : s;
+}
+
+dl_status dl_linear_swiglu(int dtype, const void* x, const void* W, const float* scales,
+                           const void* bias, void* y, float* y_f32, int M, int N, int K,
+                           void* workspace, size_t ws_bytes, void* stream) {
+    if (dtype != DL_BF16 && dtype != DL_FP8_B128)
+        return fail(DL_ERR_INVALID_ARG, "dtype %d unknown", dtype);
+    dl_status s = validate(dtype, M, N, K, x, W, scales, bias, y, y_f32);
+    if (s != DL_OK) return s;
+    if (N % 16 != 0)
+        return fail(DL_ERR_UNSUPPORTED_SHAPE, "SwiGLU needs N %% 16 == 0 (N=%d)", N);
+    if (!workspace) return fail(DL_ERR_WORKSPACE, "workspace is NULL");
+    DeviceInfo di;
+    if ((s = device_info(di)) != DL_OK) return s;
+    s = launch_layer(dtype, M, N, K, x, W, scales, bias, y, y_f32, workspace, ws_bytes,
+                     static_cast<cudaStream_t>(stream), di, false, 1);
     return s == DL_OK ? ok() : s;
 }
 
@@ -528,6 +547,10 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
     for (int i = 0; i < n_layers; ++i) {
         const dl_layer& L = layers[i];
         dl_status s = validate(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr);
+        if (s == DL_OK && L.act != 0 && L.act != 1)
+            s = fail(DL_ERR_INVALID_ARG, "act %d unknown", L.act);
+        if (s == DL_OK && L.act == 1 && L.N % 16 != 0)
+            s = fail(DL_ERR_UNSUPPORTED_SHAPE, "SwiGLU needs N %% 16 == 0 (N=%d)", L.N);
         if (s != DL_OK) {
             std::string m = g_err;
             return fail(s, "layer %d: %s", i, m.c_str());
@@ -556,7 +579,7 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
             // which never writes weights: they may prefetch their first weight
             // tiles while that kernel drains.
             dl_status r = launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y,
-                                       nullptr, workspace, ws_bytes, st, di, i > 0);
+                                       nullptr, workspace, ws_bytes, st, di, i > 0, L.act);
             if (r != DL_OK) {
                 std::string m = g_err;
                 return fail(r, "layer %d: %s", i, m.c_str());

@@ -117,6 +117,8 @@ struct LinearParams {
     int* tickets;             // [n_tiles] arrival counters (zero between calls)
     float* partials;          // [n_segments][2][MTB][kBN] fp32 (scratch)
     int M, N, K;
+    int act;                  // 0: y = x.W^T (+ bias); 1: SwiGLU over gate/up row pairs
+    int ny;                   // row stride of y (N, or N / 2 with SwiGLU)
     int KB;                   // 128-column K blocks per tile = ceil(K / 128)
     int UT;                   // partition units per tile: bf16 one K block each (UT = KB),
                               //   FP8 two (UT = ceil(KB / 2), the last one single if KB is odd)
@@ -216,7 +218,23 @@ __device__ __forceinline__ int seg_of(const LinearParams& p, long long u) {
 
 __device__ __forceinline__ void write_output(const LinearParams& p, int m, int n, float v) {
     if (p.bias) v += bf16_bits_to_f32(p.bias[n]);
-    const long long o = (long long)m * p.N + n;
+    const long long o = (long long)m * p.ny + n;
+    p.y[o] = f32_to_bf16_rne(v);
+    if (p.y_f32) p.y_f32[o] = v;
+}
+
+// SwiGLU epilogue.  The weight rows come in groups of 16: rows 16b .. 16b + 7
+// are the gate rows and rows 16b + 8 .. 16b + 15 the up rows of outputs 8b ..
+// 8b + 7.  With g and u the full fp32 sums (+ bias) of a pair,
+// y[m][j] = silu(g) * u = g / (1 + e^-g) * u, rounded once to bf16.  `ng` is
+// the gate row, j = 8 (ng / 16) + ng % 16 the output column.
+__device__ __forceinline__ void write_swiglu(const LinearParams& p, int m, int ng, float g, float u) {
+    if (p.bias) {
+        g += bf16_bits_to_f32(p.bias[ng]);
+        u += bf16_bits_to_f32(p.bias[ng + 8]);
+    }
+    const float v = g / (1.f + expf(-g)) * u;
+    const long long o = (long long)m * p.ny + (ng >> 4) * 8 + (ng & 15);
     p.y[o] = f32_to_bf16_rne(v);
     if (p.y_f32) p.y_f32[o] = v;
 }
@@ -371,7 +389,8 @@ struct SimtConsumer {
         }
     }
 
-    // Finish a run: join the accumulators and the two K halves, store the rows.
+    // Finish a run: join the accumulators and the two K halves, store the rows
+    // (SwiGLU on a finished tile: lane l < 8 pairs gate row l with up row l + 8).
     __device__ __forceinline__ void write_rows(const LinearParams& p, float* slot, int n0, int warp,
                                                int lane) {
         const int row = warp * 16 + (lane & 15);
@@ -379,7 +398,13 @@ struct SimtConsumer {
         for (int m = 0; m < MT; ++m) {
             const float mine = acc[0][m] + acc[1][m];
             const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-            if (lane < 16) put_value(p, slot, n0, m, row, mine + other);
+            const float v = mine + other;
+            if (p.act && !slot) {
+                const float up = __shfl_xor_sync(0xffffffffu, v, 8);
+                if (lane < 8 && m < p.M && n0 + row < p.N) write_swiglu(p, m, n0 + row, v, up);
+            } else if (lane < 16) {
+                put_value(p, slot, n0, m, row, v);
+            }
         }
     }
 };
@@ -554,11 +579,26 @@ struct MmaConsumer {
         }
     }
 
-    // Finish a run: add the accumulator sets and store the warp's rows.
+    // Finish a run: add the accumulator sets and store the warp's rows
+    // (SwiGLU on a finished tile: this thread holds gate row g and up row g + 8).
     __device__ __forceinline__ void write_rows(const LinearParams& p, float* slot, int n0, int warp,
                                                int lane) {
         const int g = lane >> 2, t = lane & 3;
         const int row = warp * 16 + g;
+        if (p.act && !slot) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int tok = 8 * nt + 2 * t;
+                if (n0 + row >= p.N) continue;
+                if (tok < p.M)
+                    write_swiglu(p, tok, n0 + row, acc[0][nt][0] + acc[1][nt][0],
+                                 acc[0][nt][2] + acc[1][nt][2]);
+                if (tok + 1 < p.M)
+                    write_swiglu(p, tok + 1, n0 + row, acc[0][nt][1] + acc[1][nt][1],
+                                 acc[0][nt][3] + acc[1][nt][3]);
+            }
+            return;
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int tok = 8 * nt + 2 * t;
@@ -608,6 +648,37 @@ __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int 
                 if (j0 + q <= j_last) v += val[q];       // ascending segment order
         }
         if (n0 + rr < p.N) write_output(p, m, n0 + rr, v);
+    }
+}
+
+// The same for a SwiGLU tile: each thread finishes gate row rr and its up row
+// rr + 8 (both summed in segment order) and writes one output.
+template <int MTB>
+__device__ __forceinline__ void fixup_tile_swiglu(const LinearParams& p, int tile, int j_first,
+                                                  int j_last, int tid) {
+    constexpr int kBatch = 8;
+    constexpr long long kStride = 2LL * MTB * kBN;
+    const int n0 = tile * kBN;
+    const int sl_first = (seg_begin(p, j_first) / p.UT == tile) ? 0 : 1;
+    for (int idx = tid; idx < p.M * (kBN / 2); idx += kConsumerThreads) {
+        const int m = idx / (kBN / 2), q = idx % (kBN / 2);
+        const int rr = (q >> 3) * 16 + (q & 7);                 // gate row in the tile
+        const float* first = p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN + m * kBN + rr;
+        float g = ld_cg_f32(first), u = ld_cg_f32(first + 8);
+        const float* base = p.partials + (long long)m * kBN + rr;
+        for (int j0 = j_first + 1; j0 <= j_last; j0 += kBatch) {
+            float vg[kBatch], vu[kBatch];
+#pragma unroll
+            for (int q2 = 0; q2 < kBatch; ++q2) {
+                const bool in = j0 + q2 <= j_last;
+                vg[q2] = in ? ld_cg_f32(base + (long long)(j0 + q2) * kStride) : 0.f;
+                vu[q2] = in ? ld_cg_f32(base + (long long)(j0 + q2) * kStride + 8) : 0.f;
+            }
+#pragma unroll
+            for (int q2 = 0; q2 < kBatch; ++q2)
+                if (j0 + q2 <= j_last) { g += vg[q2]; u += vu[q2]; }   // ascending segment order
+        }
+        if (n0 + rr < p.N) write_swiglu(p, m, n0 + rr, g, u);
     }
 }
 
@@ -887,7 +958,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int ft = runs[b].last;
         if (ft >= 0) {
             const long long tu0 = (long long)ft * UT;
-            fixup_tile<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + UT - 1), threadIdx.x);
+            if (p.act)
+                fixup_tile_swiglu<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + UT - 1), threadIdx.x);
+            else
+                fixup_tile<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + UT - 1), threadIdx.x);
             if (threadIdx.x == 0) p.tickets[ft] = 0;
         }
         return true;
