@@ -360,3 +360,23 @@ def test_swiglu_rows_match_the_binding_layout():
     w = dl.interleave_gate_up(gate, up)[:, 0].numpy()
     gr, ur = oracle.swiglu_rows(I)
     assert np.array_equal(w[gr], gate[:, 0].numpy()) and np.array_equal(w[ur], up[:, 0].numpy())
+
+
+# ------------------------------------------------------------------ argmax of the lm_head
+
+def test_argmax_lowest_special_cases():
+    """Ties go to the lowest index; the first NaN wins; -0 equals +0; -inf rows."""
+    v = np.array([[1.0, 3.0, 3.0, 2.0],
+                  [1.0, np.nan, 5.0, np.nan],
+                  [-0.0, 0.0, -1.0, 0.0],
+                  [-np.inf, -np.inf, -np.inf, -np.inf],
+                  [np.nan, 9.0, 1.0, 2.0],
+                  [-5.0, -2.0, -2.0, -7.0]])
+    assert oracle.argmax_lowest(v).tolist() == [1, 1, 0, 0, 0, 1]
+
+
+def test_argmax_lowest_matches_numpy_on_distinct_values():
+    """Without ties or NaN it is numpy's argmax (an independent routine)."""
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal((7, 513))
+    assert np.array_equal(oracle.argmax_lowest(v), np.argmax(v, axis=1))
