@@ -148,7 +148,8 @@ WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8
 
 def layer_specs(workload: str):
     """[(dtype, M, N, K, bias, name, act)], config id.  act = 1: gate_up with the
-    fused SwiGLU epilogue (y holds N/2 columns)."""
+    fused SwiGLU epilogue (y holds N/2 columns); act = 2: lm_head with the fused
+    argmax (y holds the M token indices, no logits are written)."""
     from weight_streaming_skinny_gb300 import inputs
     shapes = inputs.QWEN72B_SHAPES
     if workload == "qwen72b_layer_bf16_m1":
@@ -162,14 +163,29 @@ def layer_specs(workload: str):
                 specs.append((inputs.DTYPE_FP8_B128, 1, *shapes[n][:2], shapes[n][2], f"{n}.{layer}",
                               1 if n == "gate_up" else 0))
         N, K, b = inputs.QWEN72B_LM_HEAD
-        specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 0))
+        specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 2))
         return specs, 4
     raise ValueError(workload)
 
 
 def out_cols(L) -> int:
     """Columns of a layer's y (N, or N/2 with the SwiGLU epilogue)."""
-    return L.N // 2 if getattr(L, "act", 0) else L.N
+    return L.N // 2 if getattr(L, "act", 0) == 1 else L.N
+
+
+def out_buffer(L, dev):
+    """y of a layer: bf16 [M, out_cols], or int32 [M] token indices (argmax)."""
+    import torch
+    if getattr(L, "act", 0) == 2:
+        return torch.empty((L.M,), dtype=torch.int32, device=dev)
+    return torch.empty((L.M, out_cols(L)), dtype=torch.bfloat16, device=dev)
+
+
+def out_bytes(L) -> int:
+    """Algorithmic bytes of a layer: weights (+ scales) + x + its outputs (+ bias)."""
+    act = getattr(L, "act", 0)
+    y = 4 * L.M if act == 2 else 2 * L.M * out_cols(L)
+    return L.algorithmic_bytes - 2 * L.M * L.N + y
 
 
 def build_layers(workload, dev):
@@ -194,8 +210,10 @@ def build_layers(workload, dev):
 
 
 def launch(dl, L, y, ws, stream):
-    if getattr(L, "act", 0):
+    if getattr(L, "act", 0) == 1:
         dl.linear_swiglu(L.x, L.w, L.scales, L.bias, out=y, workspace=ws, stream=stream)
+    elif getattr(L, "act", 0) == 2:
+        dl.linear_argmax(L.x, L.w, L.scales, L.bias, out_idx=y, workspace=ws, stream=stream)
     elif L.dtype == "bf16":
         dl.linear_bf16(L.x, L.w, L.bias, out=y, workspace=ws, stream=stream)
     else:
@@ -214,15 +232,15 @@ def run_ours(args, rank, world, dist):
     dl.set_override({"auto": 0, "simt": 1, "mma": 2}[args.kernel], 0, 0)
     workload = args.workload
     layers = build_layers(workload, dev)
-    ys = [torch.empty((L.M, out_cols(L)), dtype=torch.bfloat16, device=dev) for _, L in layers]
+    ys = [out_buffer(L, dev) for _, L in layers]
     for j in range(1, len(layers)):
         if layers[j][1].x is None:
             layers[j][1].x = ys[j - 1]
     ws = dl.Workspace.for_shapes(
         [(L.M, L.N, L.K, dl.BF16 if L.dtype == "bf16" else dl.FP8_B128) for _, L in layers], dev)
     stream = torch.cuda.Stream(dev)
-    # algorithmic bytes; a SwiGLU layer writes M x N/2 outputs instead of M x N
-    nbytes = [L.algorithmic_bytes - (L.M * L.N if L.act else 0) for _, L in layers]
+    # algorithmic bytes (a SwiGLU layer writes M x N/2 outputs, an argmax layer M indices)
+    nbytes = [out_bytes(L) for _, L in layers]
     step_bytes = sum(nbytes)
     dl_layers = [dl.Layer(dl.BF16 if L.dtype == "bf16" else dl.FP8_B128, L.x, L.w, ys[j],
                           L.scales, L.bias, act=L.act) for j, (_, L) in enumerate(layers)]
@@ -308,9 +326,9 @@ def run_ours(args, rank, world, dist):
         chained_in = [j > 0 and layers[j][1].x is ys[j - 1] for j in range(len(layers))]
         chained_out = [j + 1 < len(layers) and chained_in[j + 1] for j in range(len(layers))]
         hx = [L.x.cpu().pin_memory() for _, L in layers]
-        hy = [torch.empty((L.M, out_cols(L)), dtype=torch.bfloat16).pin_memory() for _, L in layers]
-        h2d = sum(x.numel() * 2 for j, x in enumerate(hx) if not chained_in[j])
-        d2h = sum(y.numel() * 2 for j, y in enumerate(hy) if not chained_out[j])
+        hy = [torch.empty_like(ys[j], device="cpu").pin_memory() for j in range(len(layers))]
+        h2d = sum(x.numel() * x.element_size() for j, x in enumerate(hx) if not chained_in[j])
+        d2h = sum(y.numel() * y.element_size() for j, y in enumerate(hy) if not chained_out[j])
         E = max(3, min(K, 50))
 
         def e2e_step():
@@ -381,10 +399,10 @@ def cpu_oracle_gbs(layers_host, budget_s: float, row_frac: float = 1.0):
     prepared = []
     for name, L in layers_host:
         act = getattr(L, "act", 0)
-        ncols = L.N // 2 if act else L.N
-        n = max(1, int(ncols * row_frac))                 # outputs computed
+        ncols = L.N // 2 if act == 1 else L.N
+        n = max(1, int(ncols * row_frac))                 # outputs (or logits) computed
         cols = np.linspace(0, ncols - 1, n).astype(np.int64)
-        nw = 2 * n if act else n                          # weight rows read
+        nw = 2 * n if act == 1 else n                     # weight rows read
         xb = inputs.bf16_bits(L.x)
         bb = None if L.bias is None else inputs.bf16_bits(L.bias)
         if L.dtype == "bf16":
@@ -393,19 +411,22 @@ def cpu_oracle_gbs(layers_host, budget_s: float, row_frac: float = 1.0):
         else:
             args = (oracle.FP8_B128, xb, inputs.u8_codes(L.w), L.scales.cpu().numpy(), bb)
             wbytes = nw * L.K + 4 * ((nw + 127) // 128) * (L.K // 128)
+        ybytes = 4 * L.M if act == 2 else 2 * L.M * n
         prepared.append((args, cols, act,
-                         wbytes + 2 * L.M * L.K + 2 * L.M * n + (2 * nw if bb is not None else 0)))
+                         wbytes + 2 * L.M * L.K + ybytes + (2 * nw if bb is not None else 0)))
     threads = oracle.default_threads()
     passes, t_total, b_total = 0, 0.0, 0
     while passes == 0 or t_total < budget_s:
         for args, cols, act, b in prepared:
             a = time.perf_counter()
-            if act:
+            if act == 1:
                 oracle.swiglu(*args[:3], scales=args[3], bias_bits=args[4], outputs=cols,
                               threads=threads)
             else:
-                oracle.linear(*args[:3], scales=args[3], bias_bits=args[4], rows=cols,
-                              with_abs=False, threads=threads)
+                y = oracle.linear(*args[:3], scales=args[3], bias_bits=args[4], rows=cols,
+                                  with_abs=False, threads=threads)
+                if act == 2:
+                    oracle.argmax_lowest(y)
             t_total += time.perf_counter() - a
             b_total += b
         passes += 1
@@ -451,7 +472,8 @@ def main():
         config["layers"] = {"count": len(specs), "decoder_layers": len(specs) // 4,
                             "per_layer": [s[5].split(".")[0] + ("+swiglu" if s[6] else "")
                                           for s in specs[:4]],
-                            "dtype": specs[0][0], "M": specs[0][1], "lm_head": "bf16 152064x8192",
+                            "dtype": specs[0][0], "M": specs[0][1],
+                            "lm_head": "bf16 152064x8192 with the fused argmax (token ids, no logits)",
                             "chaining": "down -> next qkv, o -> gate_up, gate_up (SwiGLU) -> down, "
                                         "last down -> lm_head"}
 

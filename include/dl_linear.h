@@ -188,6 +188,27 @@ dl_status dl_linear_swiglu(int dtype, const void* x, const void* W, const float*
                            const void* bias, void* y, float* y_f32, int M, int N, int K,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * A linear layer (typically the lm_head) with the greedy-decoding argmax fused
+ * into its epilogue: for every row m,
+ *     idx[m] = the lowest n among the largest y[m][n] (+ bias),
+ * decided on the fp32 values before rounding; a NaN counts as larger than any
+ * number (the first NaN wins) and -0 equals +0.  This is the on-device argmax
+ * of "Developing a custom Qwen2.5 72B inference engine from scratch", §5 (pick
+ * the next token on the GPU instead of copying the logits to the host), fused
+ * into the last linear of the step: the logits need not be written at all.
+ *   dtype, x, W, scales, bias, M, N, K, workspace, ws_bytes, stream:
+ *          as for dl_linear_bf16 / dl_linear_fp8_block128
+ *   idx    int32 [M] (required, 4-byte aligned)
+ *   maxval fp32 [M] or NULL: the largest value itself
+ *   y      bf16 [M][N] or NULL; y_f32 fp32 [M][N] or NULL: the logits, if wanted
+ * Every candidate is reduced to a 64-bit key whose maximum does not depend on
+ * the order of combination, so the result is exact and reproducible.
+ */
+dl_status dl_linear_argmax(int dtype, const void* x, const void* W, const float* scales,
+                           const void* bias, int* idx, float* maxval, void* y, float* y_f32, int M,
+                           int N, int K, void* workspace, size_t ws_bytes, void* stream);
+
 /* One layer of a decode weight stream (see dl_decode_stream). */
 typedef struct dl_layer {
     int dtype;             /* dl_dtype                                    */
@@ -196,8 +217,10 @@ typedef struct dl_layer {
     const void* W;         /* bf16 [N][K] or e4m3 codes [N][K]            */
     const float* scales;   /* FP8 only: fp32 [ceil(N/128)][K/128]; else NULL */
     const void* bias;      /* bf16 [N] or NULL                            */
-    void* y;               /* bf16 [M][N], or [M][N/2] with act = 1       */
-    int act;               /* 0: plain; 1: SwiGLU (as dl_linear_swiglu)   */
+    void* y;               /* bf16 [M][N]; [M][N/2] with act = 1; int32 [M] with act = 2 */
+    int act;               /* 0: plain; 1: SwiGLU (as dl_linear_swiglu);
+                              2: argmax (as dl_linear_argmax: y receives the indices,
+                              no logits are written)                      */
 } dl_layer;
 
 /*

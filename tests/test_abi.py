@@ -9,7 +9,7 @@ import weight_streaming_skinny_gb300 as dl
 
 EXPECTED = {"dl_workspace_bytes", "dl_linear_bf16", "dl_linear_fp8_block128", "dl_decode_stream",
             "dl_graph_cache_clear", "dl_set_override", "dl_device_status", "dl_last_error",
-            "dl_version", "dl_linear_swiglu", "dl_linear_bf16_static_scratch"}
+            "dl_version", "dl_linear_swiglu", "dl_linear_bf16_static_scratch", "dl_linear_argmax"}
 
 
 def test_library_exports_every_header_symbol():
@@ -142,3 +142,16 @@ def test_interleave_gate_up_layout():
     for j in range(24):
         b, i = divmod(j, 8)
         assert torch.equal(w[16 * b + i], g[j]) and torch.equal(w[16 * b + 8 + i], u[j])
+
+
+def test_argmax_validation_before_any_cuda_call():
+    """idx is required and aligned; y may be omitted (host-side checks only)."""
+    lib = dl.load()
+    p = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 24)
+    assert lib.dl_linear_argmax(0, p, p, None, None, None, None, None, None, 1, 256, 128, ws,
+                                1 << 20, None) == 1
+    assert lib.dl_linear_argmax(0, p, p, None, None, ctypes.c_void_p((1 << 20) + 2), None, None,
+                                None, 1, 256, 128, ws, 1 << 20, None) == 3
+    assert lib.dl_linear_argmax(0, p, p, None, None, p, None, None, None, 17, 256, 128, ws,
+                                1 << 20, None) == 2

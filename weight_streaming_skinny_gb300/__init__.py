@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "BF16", "FP8_B128", "KERNEL_AUTO", "KERNEL_SIMT", "KERNEL_MMA", "DLError", "Layer",
     "library_path", "load", "version", "workspace_bytes", "Workspace", "linear_bf16",
-    "linear_swiglu", "interleave_gate_up", "ABI_VERSION",
+    "linear_swiglu", "linear_argmax", "interleave_gate_up", "ABI_VERSION",
     "linear_bf16_static_scratch", "STATIC_SCRATCH_BYTES", "WORKSPACE_ZERO_BYTES",
     "linear_fp8_block128", "decode_stream", "graph_cache_clear", "set_override",
     "device_status", "exported_symbols", "header_symbols",
@@ -84,6 +84,8 @@ def load():
         lib.dl_decode_stream.restype = i
         lib.dl_graph_cache_clear.restype = None
         lib.dl_linear_swiglu.argtypes = [i, vp, vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
+        lib.dl_linear_argmax.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
+        lib.dl_linear_argmax.restype = i
         lib.dl_linear_swiglu.restype = i
         lib.dl_set_override.argtypes = [i, i, i]
         lib.dl_set_override.restype = i
@@ -259,6 +261,43 @@ def linear_swiglu(x, w, scales=None, bias=None, *, out=None, out_f32=None,
     return out
 
 
+def linear_argmax(x, w, scales=None, bias=None, *, out_idx=None, out_max=None, out=None,
+                  out_f32=None, workspace: Workspace | None = None, stream=None):
+    """idx[M] (int32) = argmax over n of x . w^T (+ bias), lowest index among
+    ties, decided on the fp32 values (NaN largest).  out_max (fp32 [M]) gets the
+    largest value; out / out_f32 get the logits only if given."""
+    if isinstance(w, torch.Tensor) and w.dtype == torch.float8_e4m3fn:
+        w = w.view(torch.uint8)
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    fp8 = scales is not None
+    _need(w, "w", torch.uint8 if fp8 else torch.bfloat16, dev)
+    if fp8:
+        _need(scales, "scales", torch.float32, dev)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, dev)
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("x must be [M, K] and w [N, K]")
+    M, K = x.shape
+    N = w.shape[0]
+    if out_idx is None:
+        out_idx = torch.empty(M, dtype=torch.int32, device=dev)
+    _need(out_idx, "out_idx", torch.int32, dev)
+    if out_max is not None:
+        _need(out_max, "out_max", torch.float32, dev)
+    if out is not None:
+        _need(out, "out", torch.bfloat16, dev)
+    if out_f32 is not None:
+        _need(out_f32, "out_f32", torch.float32, dev)
+    dt = FP8_B128 if fp8 else BF16
+    with torch.cuda.device(dev):
+        ws = _workspace(workspace, workspace_bytes(M, N, K, dt), dev)
+        _check(load().dl_linear_argmax(dt, _ptr(x), _ptr(w), _ptr(scales), _ptr(bias), _ptr(out_idx),
+                                       _ptr(out_max), _ptr(out), _ptr(out_f32), M, N, K, ws.ptr,
+                                       ws.nbytes, _stream(stream, dev)))
+    return out_idx
+
+
 def interleave_gate_up(gate: torch.Tensor, up: torch.Tensor) -> torch.Tensor:
     """[I, K] gate and up matrices (any dtype) -> the [2I, K] row order of
     linear_swiglu: rows 16b..16b+7 = gate rows 8b..8b+7, rows 16b+8..16b+15 =
@@ -348,7 +387,8 @@ class Layer:
     y: torch.Tensor
     scales: torch.Tensor | None = None
     bias: torch.Tensor | None = None
-    act: int = 0          # 1: SwiGLU epilogue (see linear_swiglu); y is then [M, N/2]
+    act: int = 0          # 1: SwiGLU epilogue (see linear_swiglu): y is [M, N/2];
+                          # 2: argmax (see linear_argmax): y is int32 [M], no logits
 
     def shape(self):
         return (self.x.shape[0], self.w.shape[0], self.x.shape[1], self.dtype)

@@ -60,6 +60,8 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kTicketsOff = 256;
 constexpr int kMaxTiles = 16384;
 static_assert(kTicketsOff + (size_t)kMaxTiles * 4 == DL_WORKSPACE_ZERO_BYTES, "zero prefix");
+// In the first 256 bytes: int counters [0..3), then the argmax keys (16 x 8 B).
+constexpr size_t kArgmaxKeysOff = 64;
 
 struct DeviceInfo {
     bool ready = false;
@@ -328,7 +330,7 @@ dl_status validate(int dtype, int M, int N, int K, const void* x, const void* W,
 dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void* W,
                        const float* scales, const void* bias, void* y, float* y_f32,
                        void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di,
-                       bool after_own, int act) {
+                       bool after_own, int act, int* idx = nullptr, float* maxval = nullptr) {
     // after_own: every earlier kernel on the stream is one of this library's
     // (a later layer of one dl_decode_stream call), so none writes weights or
     // scales and the next one's weights may be fetched before the wait.
@@ -362,7 +364,10 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.N = N;
     p.K = K;
     p.act = act;
-    p.ny = act ? N / 2 : N;
+    p.ny = act == 1 ? N / 2 : N;
+    p.best = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + kArgmaxKeysOff);
+    p.idx = idx;
+    p.maxval = maxval;
     p.KB = pl.KB;
     p.UT = pl.UT;
     p.n_tiles = pl.n_tiles;
@@ -522,6 +527,25 @@ dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* sca
     return s == DL_OK ? ok() : s;
 }
 
+dl_status dl_linear_argmax(int dtype, const void* x, const void* W, const float* scales,
+                           const void* bias, int* idx, float* maxval, void* y, float* y_f32, int M,
+                           int N, int K, void* workspace, size_t ws_bytes, void* stream) {
+    if (dtype != DL_BF16 && dtype != DL_FP8_B128)
+        return fail(DL_ERR_INVALID_ARG, "dtype %d unknown", dtype);
+    if (!idx) return fail(DL_ERR_INVALID_ARG, "idx must be non-NULL");
+    if (!aligned(idx, 4) || (maxval && !aligned(maxval, 4)))
+        return fail(DL_ERR_MISALIGNED, "idx and maxval must be 4-byte aligned");
+    // y is optional here: validate with a stand-in when it is absent.
+    dl_status s = validate(dtype, M, N, K, x, W, scales, bias, y ? y : static_cast<void*>(idx), y_f32);
+    if (s != DL_OK) return s;
+    if (!workspace) return fail(DL_ERR_WORKSPACE, "workspace is NULL");
+    DeviceInfo di;
+    if ((s = device_info(di)) != DL_OK) return s;
+    s = launch_layer(dtype, M, N, K, x, W, scales, bias, y, y_f32, workspace, ws_bytes,
+                     static_cast<cudaStream_t>(stream), di, false, 2, idx, maxval);
+    return s == DL_OK ? ok() : s;
+}
+
 dl_status dl_linear_swiglu(int dtype, const void* x, const void* W, const float* scales,
                            const void* bias, void* y, float* y_f32, int M, int N, int K,
                            void* workspace, size_t ws_bytes, void* stream) {
@@ -547,8 +571,10 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
     for (int i = 0; i < n_layers; ++i) {
         const dl_layer& L = layers[i];
         dl_status s = validate(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr);
-        if (s == DL_OK && L.act != 0 && L.act != 1)
+        if (s == DL_OK && (L.act < 0 || L.act > 2))
             s = fail(DL_ERR_INVALID_ARG, "act %d unknown", L.act);
+        if (s == DL_OK && L.act == 2 && !aligned(L.y, 4))
+            s = fail(DL_ERR_MISALIGNED, "layer %d: the argmax indices must be 4-byte aligned", i);
         if (s == DL_OK && L.act == 1 && L.N % 16 != 0)
             s = fail(DL_ERR_UNSUPPORTED_SHAPE, "SwiGLU needs N %% 16 == 0 (N=%d)", L.N);
         if (s != DL_OK) {
@@ -578,8 +604,12 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
             // Layers after the first follow one of this library's own kernels,
             // which never writes weights: they may prefetch their first weight
             // tiles while that kernel drains.
-            dl_status r = launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y,
-                                       nullptr, workspace, ws_bytes, st, di, i > 0, L.act);
+            // act = 2: y holds the int32 argmax indices; no logits are written.
+            dl_status r = L.act == 2
+                ? launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, nullptr, nullptr,
+                               workspace, ws_bytes, st, di, i > 0, 2, static_cast<int*>(L.y), nullptr)
+                : launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr,
+                               workspace, ws_bytes, st, di, i > 0, L.act);
             if (r != DL_OK) {
                 std::string m = g_err;
                 return fail(r, "layer %d: %s", i, m.c_str());

@@ -114,10 +114,15 @@ struct LinearParams {
     const uint16_t* x;        // bf16 [M][K] (FP8: read only by units not exact in f16)
     const float* unscale;     // fp32 [KB][16] (FP8): 2^-s of the f16 copy, 0 = not exact
     int* counter;             // [0]: segments claimed after the first wave, [1]: CTAs done
+                              //   claiming, [2]: consumer warps finished (argmax)
+    unsigned long long* best; // argmax: [16] best key per token (in the zero prefix)
+    int* idx;                 // argmax: int32 [M] result
+    float* maxval;            // argmax: fp32 [M] largest logit, or null
     int* tickets;             // [n_tiles] arrival counters (zero between calls)
     float* partials;          // [n_segments][2][MTB][kBN] fp32 (scratch)
     int M, N, K;
-    int act;                  // 0: y = x.W^T (+ bias); 1: SwiGLU over gate/up row pairs
+    int act;                  // 0: y = x.W^T (+ bias); 1: SwiGLU over gate/up row pairs;
+                              //   2: also the argmax over n of every row m (see below)
     int ny;                   // row stride of y (N, or N / 2 with SwiGLU)
     int KB;                   // 128-column K blocks per tile = ceil(K / 128)
     int UT;                   // partition units per tile: bf16 one K block each (UT = KB),
@@ -165,7 +170,7 @@ struct XRows {
 // Shared-memory layout of one CTA (offsets from a 1024-aligned base).  The
 // host sizes the launch with the same function.
 struct SmemLayout {
-    int w, x, hdr, bars, runs, total;
+    int w, x, hdr, bars, runs, best, total;
 };
 
 // Hand-over of one split run between the consumer warps and the ticket warp
@@ -186,7 +191,8 @@ __host__ __device__ constexpr SmemLayout smem_layout(int dtype, int, int mt, int
     L.hdr = L.x + stages * xbytes;
     L.bars = L.hdr + stages * (int)sizeof(StageHeader);
     L.runs = L.bars + (2 * stages + 4) * 8;
-    L.total = L.runs + 2 * (int)sizeof(RunSlot) + 16;
+    L.best = L.runs + 2 * (int)sizeof(RunSlot) + 16;      // [8 warps][16 tokens] argmax keys
+    L.total = L.best + kConsumerWarps * 16 * 8;
     return L;
 }
 
@@ -216,11 +222,44 @@ __device__ __forceinline__ int seg_of(const LinearParams& p, long long u) {
 
 // ------------------------------------------------------------------ epilogue
 
-__device__ __forceinline__ void write_output(const LinearParams& p, int m, int n, float v) {
+// Final value (+ bias) of output (m, n), stored to y / y_f32 where given; the
+// value is returned for the argmax epilogue.
+__device__ __forceinline__ float write_output(const LinearParams& p, int m, int n, float v) {
     if (p.bias) v += bf16_bits_to_f32(p.bias[n]);
     const long long o = (long long)m * p.ny + n;
-    p.y[o] = f32_to_bf16_rne(v);
+    if (p.y) p.y[o] = f32_to_bf16_rne(v);
     if (p.y_f32) p.y_f32[o] = v;
+    return v;
+}
+
+// Argmax epilogue (act = 2).  A candidate (value v, index n) becomes one 64-bit
+// key whose unsigned order is the selection order: the high word orders the
+// floats (NaN above everything, -0 equal to +0), the low word is 2^32-1-n so
+// that among equal values the lowest index wins.  The maximum over keys does
+// not depend on the order candidates are combined in: results are exact and
+// reproducible.  0 is below every candidate.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
+    v += 0.f;                                            // -0 -> +0
+    const unsigned b = __float_as_uint(v);
+    const unsigned o = (v != v) ? 0xffffffffu : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
+    return ((unsigned long long)o << 32) | (0xffffffffu - (unsigned)n);
+}
+
+__device__ __forceinline__ float argmax_key_value(unsigned long long k) {
+    const unsigned o = (unsigned)(k >> 32);
+    if (o == 0xffffffffu) return __uint_as_float(0x7fffffffu);      // NaN
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+__device__ __forceinline__ unsigned long long max_u64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
+// Largest key among the lanes of `mask` reached by the xor offsets >= `from`.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k, int from) {
+#pragma unroll
+    for (int o = 16; o >= from; o >>= 1) k = max_u64(k, __shfl_xor_sync(0xffffffffu, k, o));
+    return k;
 }
 
 // SwiGLU epilogue.  The weight rows come in groups of 16: rows 16b .. 16b + 7
@@ -390,18 +429,25 @@ struct SimtConsumer {
     }
 
     // Finish a run: join the accumulators and the two K halves, store the rows
-    // (SwiGLU on a finished tile: lane l < 8 pairs gate row l with up row l + 8).
+    // (SwiGLU on a finished tile: lane l < 8 pairs gate row l with up row l + 8;
+    // argmax: the warp's best candidate per token goes to its row sbest[16]).
     __device__ __forceinline__ void write_rows(const LinearParams& p, float* slot, int n0, int warp,
-                                               int lane) {
+                                               int lane, unsigned long long* sbest) {
         const int row = warp * 16 + (lane & 15);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const float mine = acc[0][m] + acc[1][m];
             const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
             const float v = mine + other;
-            if (p.act && !slot) {
+            if (p.act == 1 && !slot) {
                 const float up = __shfl_xor_sync(0xffffffffu, v, 8);
                 if (lane < 8 && m < p.M && n0 + row < p.N) write_swiglu(p, m, n0 + row, v, up);
+            } else if (p.act == 2 && !slot) {
+                unsigned long long k = 0;
+                if (lane < 16 && m < p.M && n0 + row < p.N)
+                    k = argmax_key(write_output(p, m, n0 + row, v), n0 + row);
+                k = warp_max_key(k, 1);
+                if (lane == 0 && m < p.M) sbest[m] = max_u64(sbest[m], k);
             } else if (lane < 16) {
                 put_value(p, slot, n0, m, row, v);
             }
@@ -580,12 +626,34 @@ struct MmaConsumer {
     }
 
     // Finish a run: add the accumulator sets and store the warp's rows
-    // (SwiGLU on a finished tile: this thread holds gate row g and up row g + 8).
+    // (SwiGLU on a finished tile: this thread holds gate row g and up row g + 8;
+    // argmax: the warp's best candidate per token goes to its row sbest[16]).
     __device__ __forceinline__ void write_rows(const LinearParams& p, float* slot, int n0, int warp,
-                                               int lane) {
+                                               int lane, unsigned long long* sbest) {
         const int g = lane >> 2, t = lane & 3;
         const int row = warp * 16 + g;
-        if (p.act && !slot) {
+        if (p.act == 2 && !slot) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int tok = 8 * nt + 2 * t + tt;
+                    unsigned long long k = 0;
+                    if (tok < p.M) {
+                        if (n0 + row < p.N)
+                            k = argmax_key(write_output(p, tok, n0 + row, acc[0][nt][tt] + acc[1][nt][tt]),
+                                           n0 + row);
+                        if (n0 + row + 8 < p.N)
+                            k = max_u64(k, argmax_key(write_output(p, tok, n0 + row + 8,
+                                                                   acc[0][nt][2 + tt] + acc[1][nt][2 + tt]),
+                                                      n0 + row + 8));
+                    }
+                    k = warp_max_key(k, 4);              // over g: lanes with this t
+                    if (g == 0 && tok < p.M) sbest[tok] = max_u64(sbest[tok], k);
+                }
+            return;
+        }
+        if (p.act == 1 && !slot) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int tok = 8 * nt + 2 * t;
@@ -629,7 +697,7 @@ struct ConsumerOf<DT, kMMA, MT> {
 // stride and 16 loads are kept in flight.
 template <int MTB>
 __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int j_first, int j_last,
-                                           int tid) {
+                                           int tid, unsigned long long* sbest) {
     constexpr int kBatch = 16;
     constexpr long long kStride = 2LL * MTB * kBN;            // floats between segments' slot 0
     const int n0 = tile * kBN;
@@ -647,7 +715,15 @@ __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int 
             for (int q = 0; q < kBatch; ++q)
                 if (j0 + q <= j_last) v += val[q];       // ascending segment order
         }
-        if (n0 + rr < p.N) write_output(p, m, n0 + rr, v);
+        unsigned long long k = 0;
+        if (n0 + rr < p.N) {
+            const float vb = write_output(p, m, n0 + rr, v);
+            if (p.act == 2) k = argmax_key(vb, n0 + rr);
+        }
+        if (p.act == 2) {                                // the warp's 32 lanes share m
+            k = warp_max_key(k, 1);
+            if ((tid & 31) == 0) sbest[m] = max_u64(sbest[m], k);
+        }
     }
 }
 
@@ -708,6 +784,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     uint64_t* result = written + 2;   // [2] ticket warp -> consumer warps (count 1)
     volatile RunSlot* runs = reinterpret_cast<volatile RunSlot*>(smem + L.runs);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.runs + 2 * sizeof(RunSlot));
+    // argmax (act = 2): each consumer warp's best key per token
+    unsigned long long* sbest = reinterpret_cast<unsigned long long*>(smem + L.best) + (threadIdx.x >> 5) * 16;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
@@ -932,6 +1010,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // ---------------------------------------------------------------- consumers
     Consumer c;
     c.reset();
+    if (lane < 16) sbest[lane] = 0ull;
+    __syncwarp();
     int run_kb0 = 0;
     int n_split = 0;                  // split runs handed to the ticket warp so far
     uint32_t rph = 0u;                // phase parity of result[b] in bit b
@@ -958,10 +1038,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int ft = runs[b].last;
         if (ft >= 0) {
             const long long tu0 = (long long)ft * UT;
-            if (p.act)
+            if (p.act == 1)
                 fixup_tile_swiglu<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + UT - 1), threadIdx.x);
             else
-                fixup_tile<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + UT - 1), threadIdx.x);
+                fixup_tile<MTB>(p, ft, seg_of(p, tu0), seg_of(p, tu0 + UT - 1), threadIdx.x, sbest);
             if (threadIdx.x == 0) p.tickets[ft] = 0;
         }
         return true;
@@ -1003,7 +1083,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 const long long first_tile = seg_begin(p, seg) / UT;
                 slot = p.partials + ((long long)seg * 2 + (tile == first_tile ? 0 : 1)) * MTB * kBN;
             }
-            c.write_rows(p, slot, tile * kBN, warp, lane);
+            c.write_rows(p, slot, tile * kBN, warp, lane, sbest);
             c.reset();
             if (!whole) {
                 // Hand this run over, then settle the previous split run (its
@@ -1025,6 +1105,27 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (!*abort_flag) {
         hand_over(-1, 0, 0);
         if (n_split >= 1) settle(n_split - 1);
+    }
+    // Argmax: every consumer warp merges its per-token best into the call's keys
+    // (an atomic max: order-free); the last warp of the grid to do so turns them
+    // into indices and values and leaves the keys and its counter at zero.
+    if (p.act == 2 && !*abort_flag) {
+        __syncwarp();
+        if (lane < p.M) atomicMax(&p.best[lane], sbest[lane]);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.counter[2], 1) == (int)gridDim.x * kConsumerWarps - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            __threadfence();
+            if (lane < p.M) {
+                const unsigned long long k = atomicExch(&p.best[lane], 0ull);
+                p.idx[lane] = (int)(0xffffffffu - (unsigned)(k & 0xffffffffu));
+                if (p.maxval) p.maxval[lane] = argmax_key_value(k);
+            }
+            if (lane == 0) p.counter[2] = 0;
+        }
     }
 }
 
