@@ -192,16 +192,11 @@ def argmax_lowest(values):
     """Row-wise argmax of a [M, N] array: the lowest index n among the largest
     values, a NaN counting as larger than every number (the first NaN wins) and
     -0 equal to +0 -- greedy selection of the next token from the lm_head
-    logits.  Plain loops, float64 comparisons (exact for fp32 inputs)."""
+    logits.  Per row: the first NaN if there is one, else the first index whose
+    value equals the maximum (float64 comparisons, exact for fp32 inputs)."""
     v = np.asarray(values, dtype=np.float64)
     out = np.zeros(v.shape[0], dtype=np.int64)
     for m in range(v.shape[0]):
-        best = 0
-        for n in range(1, v.shape[1]):
-            a, b = v[m, n], v[m, best]
-            if np.isnan(b):
-                break                       # the first NaN is final
-            if np.isnan(a) or a > b:
-                best = n
-        out[m] = best
+        nan = np.flatnonzero(np.isnan(v[m]))
+        out[m] = nan[0] if nan.size else np.flatnonzero(v[m] == v[m].max())[0]
     return out
