@@ -354,4 +354,12 @@ __device__ __forceinline__ float ld_cg_f32(const float* p) {
     return v;
 }
 
+// Four floats (16-byte aligned) from L2, bypassing L1.
+__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
 }  // namespace dl

@@ -689,73 +689,128 @@ struct ConsumerOf<DT, kMMA, MT> {
 
 // ------------------------------------------------------------------ fix-up
 
-// Last arriver of a split tile: y[m][n0 + rr] = sum of the tile's partial
-// slots in segment order (+ bias, one rounding).  Every contributing slot was
-// written in this call before its ticket was taken.  Only the first
-// contributing segment can have started in an earlier tile (its slot 1); every
-// later one started in this tile (slot 0), so their slots lie at a fixed
-// stride and 16 loads are kept in flight.
+// Last arriver of a split tile: y[m][n0 + rr] = the sum, in ascending segment
+// order, of the partial rows the tile's segments j_first .. j_last stored
+// (slot 1 of j_first when that segment began in an earlier tile, else slot 0;
+// slot 0 of every later one), + bias.  The order is fixed, so the result does
+// not depend on which CTA arrives last.  All loads are issued before the first
+// add (float4 rows, up to kBatch segments in flight): one L2 round trip per
+// kBatch segments instead of one per load.  Thread tid owns rows 4 (g % 32) ..
+// + 3 of token g / 32 for g = tid (and tid + 256 when 16 tokens are staged),
+// so a warp's lanes share one token (argmax: one warp reduction per token).
 template <int MTB>
 __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int j_first, int j_last,
                                            int tid, unsigned long long* sbest) {
-    constexpr int kBatch = 16;
+    constexpr int kBatch = 8;
+    constexpr int kG = MTB > 8 ? 2 : 1;                       // row groups per thread
     constexpr long long kStride = 2LL * MTB * kBN;            // floats between segments' slot 0
     const int n0 = tile * kBN;
     const int sl_first = (seg_begin(p, j_first) / p.UT == tile) ? 0 : 1;
-    for (int idx = tid; idx < p.M * kBN; idx += kConsumerThreads) {
-        const int m = idx / kBN, rr = idx % kBN;
-        float v = ld_cg_f32(p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN + m * kBN + rr);
-        const float* base = p.partials + (long long)m * kBN + rr;
-        for (int j0 = j_first + 1; j0 <= j_last; j0 += kBatch) {
-            float val[kBatch];
+    const int nseg = j_last - j_first + 1;
+    const int ng = p.M * (kBN / 4);
+    const float* first = p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN;
+    int off[kG];
+    bool has[kG];
+    float4 v[kG];
 #pragma unroll
-            for (int q = 0; q < kBatch; ++q)
-                val[q] = (j0 + q <= j_last) ? ld_cg_f32(base + (long long)(j0 + q) * kStride) : 0.f;
+    for (int i = 0; i < kG; ++i) {
+        const int g = tid + i * kConsumerThreads;
+        has[i] = g < ng;
+        off[i] = (g >> 5) * kBN + (g & 31) * 4;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int j0 = 0; j0 < nseg; j0 += kBatch) {
+        float4 a[kG][kBatch];
 #pragma unroll
-            for (int q = 0; q < kBatch; ++q)
-                if (j0 + q <= j_last) v += val[q];       // ascending segment order
+        for (int q = 0; q < kBatch; ++q) {
+            const int j = j0 + q;
+            const float* src = j == 0 ? first : p.partials + (long long)(j_first + j) * kStride;
+#pragma unroll
+            for (int i = 0; i < kG; ++i)
+                a[i][q] = (has[i] && j < nseg) ? ld_cg_f32x4(src + off[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            if (j0 + q >= nseg) break;
+#pragma unroll
+            for (int i = 0; i < kG; ++i) {
+                if (j0 + q == 0) {
+                    v[i] = a[i][q];
+                } else {
+                    v[i].x += a[i][q].x;
+                    v[i].y += a[i][q].y;
+                    v[i].z += a[i][q].z;
+                    v[i].w += a[i][q].w;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kG; ++i) {
+        const int g = tid + i * kConsumerThreads;
+        if (g >= kG * kConsumerThreads) break;
+        const int m = g >> 5, rr = (g & 31) * 4;
+        const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
         unsigned long long k = 0;
-        if (n0 + rr < p.N) {
-            const float vb = write_output(p, m, n0 + rr, v);
-            if (p.act == 2) k = argmax_key(vb, n0 + rr);
+        if (has[i]) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (n0 + rr + c < p.N) {
+                    const float vb = write_output(p, m, n0 + rr + c, vv[c]);
+                    if (p.act == 2) k = max_u64(k, argmax_key(vb, n0 + rr + c));
+                }
+            }
         }
-        if (p.act == 2) {                                // the warp's 32 lanes share m
+        if (p.act == 2 && m < p.M) {                         // the warp's 32 lanes share m
             k = warp_max_key(k, 1);
             if ((tid & 31) == 0) sbest[m] = max_u64(sbest[m], k);
         }
     }
 }
 
-// The same for a SwiGLU tile: each thread finishes gate row rr and its up row
-// rr + 8 (both summed in segment order) and writes one output.
+// The same for a SwiGLU tile.  Thread tid < 16 M owns, for token tid / 16, the
+// gate rows 16 b + 4 h .. + 3 and their up rows (+ 8), b = (tid / 2) % 8,
+// h = tid % 2: four outputs, both sums in ascending segment order.
 template <int MTB>
 __device__ __forceinline__ void fixup_tile_swiglu(const LinearParams& p, int tile, int j_first,
                                                   int j_last, int tid) {
     constexpr int kBatch = 8;
     constexpr long long kStride = 2LL * MTB * kBN;
+    if (tid >= p.M * 16) return;
     const int n0 = tile * kBN;
     const int sl_first = (seg_begin(p, j_first) / p.UT == tile) ? 0 : 1;
-    for (int idx = tid; idx < p.M * (kBN / 2); idx += kConsumerThreads) {
-        const int m = idx / (kBN / 2), q = idx % (kBN / 2);
-        const int rr = (q >> 3) * 16 + (q & 7);                 // gate row in the tile
-        const float* first = p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN + m * kBN + rr;
-        float g = ld_cg_f32(first), u = ld_cg_f32(first + 8);
-        const float* base = p.partials + (long long)m * kBN + rr;
-        for (int j0 = j_first + 1; j0 <= j_last; j0 += kBatch) {
-            float vg[kBatch], vu[kBatch];
+    const int nseg = j_last - j_first + 1;
+    const int m = tid >> 4, rr = ((tid >> 1) & 7) * 16 + (tid & 1) * 4;
+    const int off = m * kBN + rr;
+    const float* first = p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN;
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    for (int j0 = 0; j0 < nseg; j0 += kBatch) {
+        float4 ag[kBatch], au[kBatch];
 #pragma unroll
-            for (int q2 = 0; q2 < kBatch; ++q2) {
-                const bool in = j0 + q2 <= j_last;
-                vg[q2] = in ? ld_cg_f32(base + (long long)(j0 + q2) * kStride) : 0.f;
-                vu[q2] = in ? ld_cg_f32(base + (long long)(j0 + q2) * kStride + 8) : 0.f;
-            }
-#pragma unroll
-            for (int q2 = 0; q2 < kBatch; ++q2)
-                if (j0 + q2 <= j_last) { g += vg[q2]; u += vu[q2]; }   // ascending segment order
+        for (int q = 0; q < kBatch; ++q) {
+            const int j = j0 + q;
+            const float* src = j == 0 ? first : p.partials + (long long)(j_first + j) * kStride;
+            const bool in = j < nseg;
+            ag[q] = in ? ld_cg_f32x4(src + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+            au[q] = in ? ld_cg_f32x4(src + off + 8) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        if (n0 + rr < p.N) write_swiglu(p, m, n0 + rr, g, u);
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            if (j0 + q >= nseg) break;
+            if (j0 + q == 0) {
+                g = ag[q];
+                u = au[q];
+            } else {
+                g.x += ag[q].x; g.y += ag[q].y; g.z += ag[q].z; g.w += ag[q].w;
+                u.x += au[q].x; u.y += au[q].y; u.z += au[q].z; u.w += au[q].w;
+            }
+        }
     }
+    if (n0 + rr >= p.N) return;                        // N % 16 == 0: the group is whole
+    write_swiglu(p, m, n0 + rr, g.x, u.x);
+    write_swiglu(p, m, n0 + rr + 1, g.y, u.y);
+    write_swiglu(p, m, n0 + rr + 2, g.z, u.z);
+    write_swiglu(p, m, n0 + rr + 3, g.w, u.w);
 }
 
 // ------------------------------------------------------------------ kernel
