@@ -65,13 +65,15 @@ def test_static_scratch_matches_workspace_entry_point(cuda_device):
 def test_static_scratch_rejects_oversize_plans(cuda_device):
     dl.set_override(0, 0, 0)
     K = 8192
-    for M, N in [(9, 59136), (16, 152064)]:
+    # the largest N the library takes (16,384 tiles) splits into enough segments
+    for M, N in [(9, 59136), (16, 152064), (16, 2097152)]:
         if dl.workspace_bytes(M, N, K, dl.BF16) > dl.STATIC_SCRATCH_BYTES:
             break
     else:
         pytest.skip("no candidate shape needs more scratch than the limit on this device")
-    x = torch.zeros((M, K), dtype=torch.bfloat16, device=cuda_device)
-    w = torch.zeros((N, K), dtype=torch.bfloat16, device=cuda_device)
+    # contents are never read: the plan is rejected before anything is enqueued
+    x = torch.empty((M, K), dtype=torch.bfloat16, device=cuda_device)
+    w = torch.empty((N, K), dtype=torch.bfloat16, device=cuda_device)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
     with pytest.raises(dl.DLError) as e:
         dl.linear_bf16_static_scratch(x, w, out=y)

@@ -49,6 +49,12 @@ std::atomic<int> g_cps_override{0};
 std::atomic<int> g_max_ctas_override{0};
 
 constexpr int kMaxStages = 16;
+// Work partition (see make_plan): share of the units in the first wave, the
+// smallest later segment in units, and whether later segments are aligned to
+// divisors of the units per tile.
+constexpr long long kFirstWaveNum = 7, kFirstWaveDen = 8;
+constexpr long long kMinSegUnits = 8;
+constexpr bool kAlignSegments = true;
 // Stages whose weights a single FP8 call's main kernel fetches while the prep
 // kernel runs (more delays its first activation copy).
 constexpr int kEarlyStagesAfterPrep = 3;
@@ -173,20 +179,34 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     if (grid < 1) grid = 1;
     pl.grid = (int)grid;
     // Segments (a fixed partition of the units; CTAs claim them dynamically and
-    // the fix-up sums them in segment order): a first wave of one segment per
-    // CTA holding about 5/8 of the units, then waves of `grid` segments, each
-    // covering about half of what is left, down to a minimum size that keeps
-    // the split tiles' partials cheap: at least 2 units, at most ~24 segments
-    // per tile, and partial bytes (M x 512 per segment) small next to the
-    // segment's weight bytes.
+    // the fix-up sums them in segment order).  A first wave of one segment per
+    // CTA holds about 7/8 of the units; then waves of up to `grid` segments,
+    // each covering about half of what is left, down to a minimum size `b`.
+    // Every segment that ends inside a tile costs a split run (partial rows,
+    // an arrival ticket and, for the last arrival, a fix-up), and those of the
+    // last waves land at the end of the call.  So b is large: kMinSegUnits
+    // (8 units = 256 KB of weights), at least UT/24 (at most ~24 segments per
+    // tile) and M/4 (partial bytes, M x 512 per segment, small next to the
+    // segment's weights); if UT is not a multiple of b, a divisor of UT in
+    // [b, 2b) is preferred.  When b divides UT, every later wave starts on a
+    // multiple of b (an alignment segment of fewer than b units follows the
+    // first wave if needed) and holds multiples of b: its segments end on tile
+    // boundaries or at multiples of b inside a tile.
     {
-        const long long G = pl.grid, U = pl.units;
-        long long min_seg = 2;
-        const long long by_tile = (pl.UT + 23) / 24;
+        const long long G = pl.grid, U = pl.units, UT = pl.UT;
+        long long b = kMinSegUnits;
+        const long long by_tile = (UT + 23) / 24;
         const long long by_m = (M + 3) / 4;
-        if (by_tile > min_seg) min_seg = by_tile;
-        if (by_m > min_seg) min_seg = by_m;
-        long long s0 = (U * 5 / 8) / G;
+        if (by_tile > b) b = by_tile;
+        if (by_m > b) b = by_m;
+        if (kAlignSegments && UT % b != 0)
+            for (long long d = b; d < 2 * b; ++d)
+                if (UT % d == 0) {
+                    b = d;
+                    break;
+                }
+        const bool aligned = kAlignSegments && UT % b == 0;
+        long long s0 = (U * kFirstWaveNum / kFirstWaveDen) / G;
         if (s0 < 1) s0 = 1;
         int w = 0;
         pl.wave_seg0[0] = 0;
@@ -194,10 +214,21 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
         pl.wave_size[0] = (int)s0;
         long long seg = G, unit = G * s0;
         ++w;
+        if (aligned && unit < U && unit % b != 0) {
+            long long a = b - unit % b;
+            if (a > U - unit) a = U - unit;
+            pl.wave_seg0[w] = (int)seg;
+            pl.wave_unit0[w] = unit;
+            pl.wave_size[w] = (int)a;
+            seg += 1;
+            unit += a;
+            ++w;
+        }
         while (unit < U) {
             const long long rem = U - unit;
             long long size = rem / (2 * G);
-            if (size < min_seg) size = min_seg;
+            if (aligned) size -= size % b;
+            if (size < b) size = b;
             if (w == dl::kMaxWaves - 1) size = (rem + G - 1) / G;   // last wave takes the rest
             long long count = (rem + size - 1) / size;
             if (count > G) count = G;
