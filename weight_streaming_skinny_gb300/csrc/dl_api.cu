@@ -55,6 +55,7 @@ constexpr int kMaxStages = 16;
 constexpr long long kFirstWaveNum = 7, kFirstWaveDen = 8;
 constexpr long long kMinSegUnits = 8;
 constexpr bool kAlignSegments = true;
+constexpr long long kMinLastSegFp8 = 4;
 // Stages whose weights a single FP8 call's main kernel fetches while the prep
 // kernel runs (more delays its first activation copy).
 constexpr int kEarlyStagesAfterPrep = 3;
@@ -228,7 +229,17 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
             const long long rem = U - unit;
             long long size = rem / (2 * G);
             if (aligned) size -= size % b;
-            if (size < b) size = b;
+            if (size < b) {
+                size = b;
+                // FP8 (twice the multiply-adds per byte, so a split run costs
+                // relatively less): once fewer than G x b units are left, one
+                // segment per CTA (at least kMinLastSegFp8 units), so that the
+                // last wave keeps every SM streaming.
+                if (dtype == DL_FP8_B128 && rem < G * b) {
+                    size = (rem + G - 1) / G;
+                    if (size < kMinLastSegFp8) size = kMinLastSegFp8;
+                }
+            }
             if (w == dl::kMaxWaves - 1) size = (rem + G - 1) / G;   // last wave takes the rest
             long long count = (rem + size - 1) / size;
             if (count > G) count = G;
