@@ -143,7 +143,11 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workloads
 
-WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8_m1"]
+MLP_TOKENS = (1, 2, 4, 6, 8, 16)
+# The token sweep: the two largest linears of a decoder layer (gate_up, down)
+# at M = 1..16 tokens, each dtype.
+WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8_m1"] + [
+    f"qwen72b_mlp_{dt}_m{m}" for dt in ("bf16", "fp8") for m in MLP_TOKENS]
 
 
 def layer_specs(workload: str):
@@ -165,6 +169,10 @@ def layer_specs(workload: str):
         N, K, b = inputs.QWEN72B_LM_HEAD
         specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 2))
         return specs, 4
+    if workload.startswith("qwen72b_mlp_"):
+        _, _, dt, m = workload.split("_")
+        dtype = inputs.DTYPE_BF16 if dt == "bf16" else inputs.DTYPE_FP8_B128
+        return [(dtype, int(m[1:]), *shapes[n][:2], shapes[n][2], n, 0) for n in ("gate_up", "down")], 3
     raise ValueError(workload)
 
 
@@ -464,8 +472,8 @@ def main():
     config = {"workload": args.workload,
               "layers": [{"name": s[5], "dtype": s[0], "M": s[1], "N": s[2], "K": s[3],
                           "bias": s[4]} for s in specs],
-              "l2": "inputs larger than L2: every step streams all four weight matrices "
-                    "(>= 0.88 GB) through a 129 MB L2",
+              "l2": "inputs larger than L2: every step streams every weight matrix of the "
+                    "workload (each step >= 0.7 GB) through a 129 MB L2",
               "parallelism": f"replicas x{world}", "kernel_family": args.kernel,
               "mode": args.mode}
     if len(specs) > 8:
