@@ -244,16 +244,18 @@ def run_ours(args, rank, world, dist):
     for j in range(1, len(layers)):
         if layers[j][1].x is None:
             layers[j][1].x = ys[j - 1]
-    ws = dl.Workspace.for_shapes(
-        [(L.M, L.N, L.K, dl.BF16 if L.dtype == "bf16" else dl.FP8_B128) for _, L in layers], dev)
     stream = torch.cuda.Stream(dev)
     # algorithmic bytes (a SwiGLU layer writes M x N/2 outputs, an argmax layer M indices)
     nbytes = [out_bytes(L) for _, L in layers]
     step_bytes = sum(nbytes)
     dl_layers = [dl.Layer(dl.BF16 if L.dtype == "bf16" else dl.FP8_B128, L.x, L.w, ys[j],
                           L.scales, L.bias, act=L.act) for j, (_, L) in enumerate(layers)]
-    # kernels per step: one per layer, two for FP8 (activation prep + main)
-    launches_per_step = sum(1 if L.dtype == "bf16" else 2 for _, L in layers)
+    # the stream's workspace: room for the up-front FP8 activation copies
+    ws = dl.Workspace.for_stream(dl_layers)
+    # kernels per step: calls mode one per layer plus a prep per FP8 layer; else
+    # the library's own count for the stream (prep launches included)
+    launches_per_step = (sum(1 if L.dtype == "bf16" else 2 for _, L in layers) if args.mode == "calls"
+                         else dl.decode_stream_launches(dl_layers, ws))
     use_graph = args.mode == "graph"
     torch.cuda.synchronize(dev)
 

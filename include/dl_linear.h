@@ -239,6 +239,27 @@ typedef struct dl_layer {
 dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace,
                            size_t ws_bytes, void* stream, int use_graph);
 
+/*
+ * Workspace bytes for which dl_decode_stream makes ahead the activation
+ * copies of every FP8 layer among the first 16 whose x no earlier layer of
+ * the list writes (no byte of its x lies in an earlier layer's y): layer 0's
+ * just before it, the others in a launch that runs alongside layer 0 (or, if
+ * layer 0 is not such a layer, before it), so that those layers follow one
+ * another without a prep kernel in between: the largest layer's
+ * dl_workspace_bytes plus one region per such layer.  With a
+ * smaller workspace (at least the largest layer's) the call is still correct;
+ * layers whose copy does not fit are prepared one by one.  0 if the list is
+ * invalid.  Host-only apart from reading device attributes.
+ */
+size_t dl_decode_stream_workspace_bytes(const dl_layer* layers, int n_layers);
+
+/*
+ * Kernel launches one dl_decode_stream call over this list enqueues with a
+ * workspace of ws_bytes (prep launches included), or -1 if the list is
+ * invalid.  Host-only apart from reading device attributes.
+ */
+int dl_decode_stream_launches(const dl_layer* layers, int n_layers, size_t ws_bytes);
+
 /* Destroy every cached graph (host call; synchronises nothing). */
 void dl_graph_cache_clear(void);
 

@@ -9,7 +9,8 @@ import weight_streaming_skinny_gb300 as dl
 
 EXPECTED = {"dl_workspace_bytes", "dl_linear_bf16", "dl_linear_fp8_block128", "dl_decode_stream",
             "dl_graph_cache_clear", "dl_set_override", "dl_device_status", "dl_last_error",
-            "dl_version", "dl_linear_swiglu", "dl_linear_bf16_static_scratch", "dl_linear_argmax"}
+            "dl_version", "dl_linear_swiglu", "dl_linear_bf16_static_scratch", "dl_linear_argmax",
+            "dl_decode_stream_workspace_bytes", "dl_decode_stream_launches"}
 
 
 def test_library_exports_every_header_symbol():

@@ -22,7 +22,9 @@ __all__ = [
     "library_path", "load", "version", "workspace_bytes", "Workspace", "linear_bf16",
     "linear_swiglu", "linear_argmax", "interleave_gate_up", "ABI_VERSION",
     "linear_bf16_static_scratch", "STATIC_SCRATCH_BYTES", "WORKSPACE_ZERO_BYTES",
-    "linear_fp8_block128", "decode_stream", "graph_cache_clear", "set_override",
+    "linear_fp8_block128", "decode_stream", "decode_stream_workspace_bytes",
+    "decode_stream_launches", "graph_cache_clear",
+    "set_override",
     "device_status", "exported_symbols", "header_symbols",
 ]
 
@@ -83,6 +85,10 @@ def load():
         lib.dl_decode_stream.argtypes = [ctypes.POINTER(_Layer), i, vp, sz, vp, i]
         lib.dl_decode_stream.restype = i
         lib.dl_graph_cache_clear.restype = None
+        lib.dl_decode_stream_workspace_bytes.argtypes = [ctypes.POINTER(_Layer), i]
+        lib.dl_decode_stream_workspace_bytes.restype = sz
+        lib.dl_decode_stream_launches.argtypes = [ctypes.POINTER(_Layer), i, sz]
+        lib.dl_decode_stream_launches.restype = i
         lib.dl_linear_swiglu.argtypes = [i, vp, vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
         lib.dl_linear_argmax.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, vp, sz, vp]
         lib.dl_linear_argmax.restype = i
@@ -168,6 +174,13 @@ class Workspace:
         with torch.cuda.device(torch.device(device)):
             n = max(workspace_bytes(*s) for s in shapes)
         return cls(n, device)
+
+    @classmethod
+    def for_stream(cls, layers, device=None):
+        """Workspace with which decode_stream makes the activation copies of all
+        FP8 layers whose x no earlier layer writes in one launch at the start."""
+        n = decode_stream_workspace_bytes(layers)
+        return cls(n, device if device is not None else layers[0].x.device)
 
     def reset(self):
         self.tensor.zero_()
@@ -412,6 +425,29 @@ def decode_stream(layers, workspace: Workspace, *, use_graph: bool = False, stre
     with torch.cuda.device(dev):
         _check(load().dl_decode_stream(arr, len(layers), workspace.ptr, workspace.nbytes,
                                        _stream(stream, dev), 1 if use_graph else 0))
+
+
+def decode_stream_workspace_bytes(layers) -> int:
+    """Workspace bytes for decode_stream over `layers` with every FP8 layer whose
+    x is ready at the start prepared in one launch (see dl_linear.h)."""
+    arr = (_Layer * max(1, len(layers)))(*[_layer_struct(L) for L in layers])
+    dev = layers[0].x.device if layers else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        n = load().dl_decode_stream_workspace_bytes(arr, len(layers))
+    if n == 0:
+        raise ValueError("invalid layer list: " + load().dl_last_error().decode())
+    return n
+
+
+def decode_stream_launches(layers, workspace: Workspace) -> int:
+    """Kernels one decode_stream call over `layers` enqueues with this workspace."""
+    arr = (_Layer * max(1, len(layers)))(*[_layer_struct(L) for L in layers])
+    dev = layers[0].x.device if layers else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        n = load().dl_decode_stream_launches(arr, len(layers), workspace.nbytes)
+    if n < 0:
+        raise ValueError("invalid layer list: " + load().dl_last_error().decode())
+    return n
 
 
 def graph_cache_clear():

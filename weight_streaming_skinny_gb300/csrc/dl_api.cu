@@ -56,6 +56,9 @@ constexpr long long kFirstWaveNum = 7, kFirstWaveDen = 8;
 constexpr long long kMinSegUnits = 8;
 constexpr bool kAlignSegments = true;
 constexpr long long kMinLastSegFp8 = 4;
+// Layers of a stream whose FP8 activation copies may be made ahead (a bounded
+// amount of up-front work and workspace).
+constexpr int kHoistWindow = 16;
 // Stages whose weights a single FP8 call's main kernel fetches while the prep
 // kernel runs (more delays its first activation copy).
 constexpr int kEarlyStagesAfterPrep = 3;
@@ -372,10 +375,13 @@ dl_status validate(int dtype, int M, int N, int K, const void* x, const void* W,
 dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void* W,
                        const float* scales, const void* bias, void* y, float* y_f32,
                        void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di,
-                       bool after_own, int act, int* idx = nullptr, float* maxval = nullptr) {
+                       bool after_own, int act, int* idx = nullptr, float* maxval = nullptr,
+                       uint16_t* xh_ready = nullptr, float* unscale_ready = nullptr) {
     // after_own: every earlier kernel on the stream is one of this library's
     // (a later layer of one dl_decode_stream call), so none writes weights or
     // scales and the next one's weights may be fetched before the wait.
+    // xh_ready / unscale_ready (FP8): the activation copy was already written
+    // there by an earlier prep launch of the same stream; no prep here.
     Plan pl;
     dl_status s = make_plan(dtype, M, N, K, di, pl);
     if (s != DL_OK) return s;
@@ -389,6 +395,11 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     char* wsb = static_cast<char*>(ws);
     uint16_t* xh = dtype == DL_FP8_B128 ? reinterpret_cast<uint16_t*>(wsb + pl.xh_off) : nullptr;
     float* unscale = dtype == DL_FP8_B128 ? reinterpret_cast<float*>(wsb + pl.unscale_off) : nullptr;
+    const bool prepped = dtype == DL_FP8_B128 && xh_ready && unscale_ready;
+    if (prepped) {
+        xh = xh_ready;
+        unscale = unscale_ready;
+    }
     CUtensorMap tw, tx;
     if ((s = encode_maps(pl, M, N, K, xh ? static_cast<const void*>(xh) : x, W, tw, tx)) != DL_OK)
         return s;
@@ -438,9 +449,12 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
         // so main fills its whole ring during the previous layer's tail.
         p.early_stages = after_own ? pl.stages : kEarlyStagesAfterPrep;
         e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, false);
-        if (e == cudaSuccess)
-            e = dl::launch_prep_x(static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, pl.mtb,
-                                  after_own, stream);
+        if (e == cudaSuccess && !prepped) {
+            dl::PrepBatch b{};
+            b.n = 1;
+            b.layer[0] = dl::PrepLayer{static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, pl.mtb, 0};
+            e = dl::launch_prep_x(b, after_own, stream);
+        }
         if (e == cudaSuccess)
             e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
     }
@@ -483,6 +497,73 @@ dl_status static_scratch(void** out) {
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];
+    return DL_OK;
+}
+
+// ----------------------------------------------------------------- stream planning
+
+// Validation of one dl_decode_stream layer (host-only).
+dl_status validate_layer(const dl_layer& L, int i) {
+    dl_status s = validate(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr);
+    if (s == DL_OK && (L.act < 0 || L.act > 2))
+        s = fail(DL_ERR_INVALID_ARG, "act %d unknown", L.act);
+    if (s == DL_OK && L.act == 2 && !aligned(L.y, 4))
+        s = fail(DL_ERR_MISALIGNED, "the argmax indices must be 4-byte aligned");
+    if (s == DL_OK && L.act == 1 && L.N % 16 != 0)
+        s = fail(DL_ERR_UNSUPPORTED_SHAPE, "SwiGLU needs N %% 16 == 0 (N=%d)", L.N);
+    if (s != DL_OK) {
+        std::string m = g_err;
+        return fail(s, "layer %d: %s", i, m.c_str());
+    }
+    return DL_OK;
+}
+
+// Bytes of y a layer writes (bf16 [M][N or N/2], or int32 [M] indices).
+size_t y_bytes(const dl_layer& L) {
+    if (L.act == 2) return (size_t)4 * L.M;
+    return (size_t)2 * L.M * (L.act == 1 ? L.N / 2 : L.N);
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+// The workspace the layers need one at a time (the largest single plan), and
+// where the FP8 layers among the first kHoistWindow whose activations are
+// ready when the stream starts -- no earlier layer of the stream writes any
+// byte of their x -- keep their f16 copies: one region each after that, so
+// that the copies are made ahead and those layers then follow one another
+// like bf16 layers.  `limit` = the caller's workspace (0: no limit); layers
+// that do not fit get their own prep launch as usual.  off[i] = 0: not
+// hoisted.
+dl_status plan_stream(const dl_layer* layers, int n, const DeviceInfo& di, size_t limit,
+                      size_t& base, std::vector<size_t>& off, size_t& end) {
+    base = 0;
+    for (int i = 0; i < n; ++i) {
+        Plan pl;
+        dl_status s = make_plan(layers[i].dtype, layers[i].M, layers[i].N, layers[i].K, di, pl);
+        if (s != DL_OK) return s;
+        base = pl.ws_bytes > base ? pl.ws_bytes : base;
+    }
+    off.assign((size_t)n, 0);
+    end = align_up(base, 256);
+    for (int i = 0; i < n && i < kHoistWindow; ++i) {
+        const dl_layer& L = layers[i];
+        if (L.dtype != DL_FP8_B128) continue;
+        bool ready = true;
+        const size_t xb = (size_t)2 * L.M * L.K;
+        for (int j = 0; j < i && ready; ++j) ready = !overlaps(L.x, xb, layers[j].y, y_bytes(layers[j]));
+        if (!ready) continue;
+        Plan pl;
+        dl_status s = make_plan(L.dtype, L.M, L.N, L.K, di, pl);
+        if (s != DL_OK) return s;
+        const size_t need = align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256) +
+                            align_up((size_t)pl.KB * dl::kUnscaleStride * sizeof(float), 256);
+        if (limit && end + need > limit) continue;
+        off[(size_t)i] = end;
+        end += need;
+    }
     return DL_OK;
 }
 
@@ -611,18 +692,8 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
         return fail(DL_ERR_INVALID_ARG, "layers must be non-NULL when n_layers > 0");
     if (use_graph != 0 && use_graph != 1) return fail(DL_ERR_INVALID_ARG, "use_graph must be 0 or 1");
     for (int i = 0; i < n_layers; ++i) {
-        const dl_layer& L = layers[i];
-        dl_status s = validate(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr);
-        if (s == DL_OK && (L.act < 0 || L.act > 2))
-            s = fail(DL_ERR_INVALID_ARG, "act %d unknown", L.act);
-        if (s == DL_OK && L.act == 2 && !aligned(L.y, 4))
-            s = fail(DL_ERR_MISALIGNED, "layer %d: the argmax indices must be 4-byte aligned", i);
-        if (s == DL_OK && L.act == 1 && L.N % 16 != 0)
-            s = fail(DL_ERR_UNSUPPORTED_SHAPE, "SwiGLU needs N %% 16 == 0 (N=%d)", L.N);
-        if (s != DL_OK) {
-            std::string m = g_err;
-            return fail(s, "layer %d: %s", i, m.c_str());
-        }
+        dl_status s = validate_layer(layers[i], i);
+        if (s != DL_OK) return s;
     }
     if (n_layers == 0) return ok();
     if (!workspace) return fail(DL_ERR_WORKSPACE, "workspace is NULL");
@@ -639,23 +710,83 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
                         pl.ws_bytes, ws_bytes);
         if ((s = prepare_layer(L.dtype, L.M, L.N, L.K, di)) != DL_OK) return s;
     }
+    size_t base = 0, end = 0;
+    std::vector<size_t> hoist;
+    if ((s = plan_stream(layers, n_layers, di, ws_bytes, base, hoist, end)) != DL_OK) return s;
+    char* wsb = static_cast<char*>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto enqueue_all = [&]() -> dl_status {
+        // The activation copies of the FP8 layers whose x is ready at the
+        // start (hoist[i] != 0): layer 0's alone before it (it waits for the
+        // kernels before the stream, and only then lets layer 0 launch); every
+        // later one's in launches of up to kMaxPrepLayers placed right after
+        // layer 0's kernel, which copy while it runs and complete only after
+        // it (wait_last).
+        bool any = false;
+        auto region = [&](int i, const Plan& pl, uint16_t*& xh, float*& us) {
+            xh = reinterpret_cast<uint16_t*>(wsb + hoist[(size_t)i]);
+            us = reinterpret_cast<float*>(wsb + hoist[(size_t)i] +
+                                          align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256));
+        };
+        auto enqueue_copies = [&](int from, int to, bool wait_last) -> dl_status {
+            dl::PrepBatch b{};
+            b.wait_last = wait_last ? 1 : 0;
+            for (int i = from; i < to; ++i) {
+                if (!hoist[(size_t)i]) continue;
+                const dl_layer& L = layers[i];
+                Plan pl;
+                dl_status r = make_plan(L.dtype, L.M, L.N, L.K, di, pl);
+                if (r != DL_OK) return r;
+                uint16_t* xh;
+                float* us;
+                region(i, pl, xh, us);
+                b.layer[b.n++] = dl::PrepLayer{static_cast<const uint16_t*>(L.x), xh, us, L.M, L.K, pl.KB, pl.mtb, 0};
+                if (b.n == dl::kMaxPrepLayers || i == to - 1) {
+                    const cudaError_t e = dl::launch_prep_x(b, false, st);
+                    if (e != cudaSuccess) return fail(DL_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
+                    any = true;
+                    b.n = 0;
+                }
+            }
+            if (b.n) {
+                const cudaError_t e = dl::launch_prep_x(b, false, st);
+                if (e != cudaSuccess) return fail(DL_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
+                any = true;
+            }
+            return DL_OK;
+        };
+        // If layer 0 has no copy of its own made here, its kernel may let the
+        // next one start before the kernels before the stream are done: the
+        // copies then all go before it, waiting first.
+        const bool split = hoist[0] != 0;
+        dl_status r0 = enqueue_copies(0, split ? 1 : n_layers, false);
+        if (r0 != DL_OK) return r0;
         for (int i = 0; i < n_layers; ++i) {
             const dl_layer& L = layers[i];
-            // Layers after the first follow one of this library's own kernels,
-            // which never writes weights: they may prefetch their first weight
-            // tiles while that kernel drains.
+            // Layers after the first, or after a prep launch, follow one of this
+            // library's own kernels, which never writes weights: they may
+            // prefetch their first weight tiles while that kernel drains.
+            const bool after_own = i > 0 || any;
+            uint16_t* xh = nullptr;
+            float* us = nullptr;
+            if (hoist[(size_t)i]) {
+                Plan pl;
+                dl_status r = make_plan(L.dtype, L.M, L.N, L.K, di, pl);
+                if (r != DL_OK) return r;
+                region(i, pl, xh, us);
+            }
             // act = 2: y holds the int32 argmax indices; no logits are written.
             dl_status r = L.act == 2
                 ? launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, nullptr, nullptr,
-                               workspace, ws_bytes, st, di, i > 0, 2, static_cast<int*>(L.y), nullptr)
+                               workspace, ws_bytes, st, di, after_own, 2, static_cast<int*>(L.y),
+                               nullptr, xh, us)
                 : launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr,
-                               workspace, ws_bytes, st, di, i > 0, L.act);
+                               workspace, ws_bytes, st, di, after_own, L.act, nullptr, nullptr, xh, us);
             if (r != DL_OK) {
                 std::string m = g_err;
                 return fail(r, "layer %d: %s", i, m.c_str());
             }
+            if (i == 0 && split && (r = enqueue_copies(1, n_layers, true)) != DL_OK) return r;
         }
         return DL_OK;
     };
@@ -699,6 +830,40 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
     if ((e = cudaGraphLaunch(exec, st)) != cudaSuccess)
         return fail(DL_ERR_CUDA, "cudaGraphLaunch: %s", cudaGetErrorString(e));
     return ok();
+}
+
+size_t dl_decode_stream_workspace_bytes(const dl_layer* layers, int n_layers) {
+    if (n_layers <= 0 || !layers) return 0;
+    for (int i = 0; i < n_layers; ++i)
+        if (validate_layer(layers[i], i) != DL_OK) return 0;
+    DeviceInfo di;
+    if (device_info(di) != DL_OK) return 0;
+    size_t base = 0, end = 0;
+    std::vector<size_t> hoist;
+    if (plan_stream(layers, n_layers, di, 0, base, hoist, end) != DL_OK) return 0;
+    return end > base ? end : base;
+}
+
+int dl_decode_stream_launches(const dl_layer* layers, int n_layers, size_t ws_bytes) {
+    if (n_layers < 0 || (n_layers > 0 && !layers)) return -1;
+    if (n_layers == 0) return 0;
+    for (int i = 0; i < n_layers; ++i)
+        if (validate_layer(layers[i], i) != DL_OK) return -1;
+    DeviceInfo di;
+    if (device_info(di) != DL_OK) return -1;
+    size_t base = 0, end = 0;
+    std::vector<size_t> hoist;
+    if (plan_stream(layers, n_layers, di, ws_bytes, base, hoist, end) != DL_OK) return -1;
+    int later = 0, fp8 = 0;
+    for (int i = 0; i < n_layers; ++i) {
+        fp8 += layers[i].dtype == DL_FP8_B128;
+        later += i > 0 && hoist[(size_t)i] != 0;
+    }
+    const int first = hoist[0] != 0;
+    // layer 0's copy, the other copies (kMaxPrepLayers per launch), one main
+    // kernel per layer, and a prep kernel before every other FP8 layer
+    return first + (later + dl::kMaxPrepLayers - 1) / dl::kMaxPrepLayers + n_layers +
+           (fp8 - first - later);
 }
 
 void dl_graph_cache_clear(void) {

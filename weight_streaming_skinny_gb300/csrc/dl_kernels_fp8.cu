@@ -20,20 +20,21 @@ namespace dl {
 // ldmatrix of a token row then yields the B fragment that matches the e4m3
 // codes 4t .. 4t + 3 a thread receives for the A operand.
 // One warp per (block, token slot); lane l handles 4 values.  K % 128 == 0.
-__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict__ x,
-                                                     uint16_t* __restrict__ xh,
-                                                     float* __restrict__ unscale, int M, int K,
-                                                     int KB, int mtb, int early_trigger) {
-    // x may be the previous kernel's output: wait for it.  The main kernel that
-    // follows prefetches weights as soon as this grid lets it launch, so unless
-    // every kernel before is known never to write weights (early_trigger, inside
-    // one decode stream) it is let launch only after that wait.
-    if (early_trigger) griddep_launch_dependents();
-    griddep_wait();
-    if (!early_trigger) griddep_launch_dependents();
-    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    const int kb = w / kUnscaleStride, tok = w % kUnscaleStride;
-    if (kb >= KB) return;
+// One launch covers up to kMaxPrepLayers layers (blockIdx.y = layer): the
+// copies of every layer of a decode stream whose x is ready when the stream
+// starts.
+// The four x values lane `lane` of a pair's warp converts (zero for the token
+// slots >= M).
+__device__ __forceinline__ uint2 load_pair(const PrepLayer& L, int kb, int tok, int lane) {
+    if (tok >= L.M) return make_uint2(0u, 0u);
+    return ldg64(L.x + (long long)tok * L.K + (long long)kb * kBK + lane * 4);
+}
+
+// One pair: this warp's (K block, token slot) of layer L, from its values v.
+__device__ __forceinline__ void prep_pair(const PrepLayer& L, int kb, int tok, int lane, uint2 v) {
+    uint16_t* __restrict__ xh = L.xh;
+    float* __restrict__ unscale = L.unscale;
+    const int M = L.M, mtb = L.mtb;
     // This lane's 4 columns 4t .. 4t + 3 (t = lane % 4) of 16-column group
     // (lane % 16) / 4 of half lane / 16 go to positions 2t, 2t + 1 and
     // 2t + 8, 2t + 9 of that group.
@@ -48,7 +49,6 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict_
         if (lane == 0) unscale[kb * kUnscaleStride + tok] = 1.f;
         return;
     }
-    const uint2 v = ldg64(x + (long long)tok * K + (long long)kb * kBK + lane * 4);
     const uint32_t b[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
     unsigned emax = 0, emin = 255;
     bool bad = false;
@@ -75,6 +75,59 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* __restrict_
             !ok ? 0.f : (emax ? __uint_as_float((emax - 14u) << 23) : 1.f);
 }
 
+template <int NB>
+__global__ void __launch_bounds__(256) prep_x_kernel(const __grid_constant__ PrepBatchN<NB> batch) {
+    const int lane = threadIdx.x & 31;
+    // (single-layer launches never copy ahead: that code is left out of them)
+    if (NB > 1 && batch.wait_last) {
+        // x is ready already (see PrepBatch): copy it while the previous
+        // kernel runs, then complete only after that kernel has (every thread
+        // waits), so that a kernel waiting for this grid also waits for it.
+        // A small grid (at most one block per SM) walks all layers' pairs,
+        // kPrepInFlight loads in flight per warp, so that its waiting blocks
+        // leave room for the next kernel's CTAs.
+        griddep_launch_dependents();
+        const int nw = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
+        const int total = batch.layer[batch.n - 1].pair0 + batch.layer[batch.n - 1].KB * kUnscaleStride;
+        for (int q0 = w0; q0 < total; q0 += nw * kPrepInFlight) {
+            uint2 v[kPrepInFlight];
+            int li[kPrepInFlight];
+#pragma unroll
+            for (int i = 0; i < kPrepInFlight; ++i) {
+                const int q = q0 + i * nw;
+                int l = 0;
+                while (l + 1 < batch.n && batch.layer[l + 1].pair0 <= q) ++l;
+                li[i] = l;
+                const int r = q - batch.layer[l].pair0;
+                v[i] = q < total ? load_pair(batch.layer[l], r / kUnscaleStride, r % kUnscaleStride, lane)
+                                 : make_uint2(0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < kPrepInFlight; ++i) {
+                const int q = q0 + i * nw;
+                if (q >= total) break;
+                const int r = q - batch.layer[li[i]].pair0;
+                prep_pair(batch.layer[li[i]], r / kUnscaleStride, r % kUnscaleStride, lane, v[i]);
+            }
+        }
+        griddep_wait();
+        return;
+    }
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int kb = w / kUnscaleStride, tok = w % kUnscaleStride;
+    const bool mine = (int)blockIdx.y < batch.n && kb < batch.layer[blockIdx.y].KB;
+    // x may be the previous kernel's output: wait for it.  The main kernel that
+    // follows prefetches weights as soon as this grid lets it launch, so unless
+    // every kernel before is known never to write weights (early_trigger, inside
+    // one decode stream) it is let launch only after that wait.
+    if (batch.early_trigger) griddep_launch_dependents();
+    griddep_wait();
+    if (!batch.early_trigger) griddep_launch_dependents();
+    if (mine) {
+        const PrepLayer& L = batch.layer[blockIdx.y];
+        prep_pair(L, kb, tok, lane, load_pair(L, kb, tok, lane));
+    }
+}
 
 cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const CUtensorMap& tx,
                               const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
@@ -82,11 +135,32 @@ cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const C
     return launch_family<kFP8>(family, mt, tw, tx, p, grid, smem, stream, launch);
 }
 
-cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M, int K, int KB,
-                          int mtb, bool early_trigger, cudaStream_t stream) {
-    // One warp per (k-block, token slot), 8 warps per block.
+// One layer per launch passes a small parameter block (NB = 1); batches up to
+// kMaxPrepLayers.
+template <int NB>
+static cudaError_t launch_prep_n(const PrepBatch& b, bool early_trigger, cudaStream_t stream) {
+    // One warp per (k-block, token slot), 8 warps per block; one grid row per layer.
+    PrepBatchN<NB> bb{};
+    bb.n = b.n;
+    bb.early_trigger = early_trigger ? 1 : 0;
+    bb.wait_last = b.wait_last;
+    int most = 1, total = 0;
+    for (int i = 0; i < b.n; ++i) {
+        bb.layer[i] = b.layer[i];
+        bb.layer[i].pair0 = total;
+        total += b.layer[i].KB * kUnscaleStride;
+        const int blocks = (b.layer[i].KB * kUnscaleStride + 7) / 8;
+        most = blocks > most ? blocks : most;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((KB * kUnscaleStride + 7) / 8));
+    cfg.gridDim = dim3((unsigned)most, (unsigned)b.n);
+    if (b.wait_last) {
+        int sms = 0, dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int blocks = (total + 7) / 8;
+        cfg.gridDim = dim3((unsigned)(blocks < sms ? blocks : sms), 1u);
+    }
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -95,10 +169,15 @@ cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e =
-        cudaLaunchKernelEx(&cfg, prep_x_kernel, x, xh, unscale, M, K, KB, mtb, early_trigger ? 1 : 0);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prep_x_kernel<NB>, bb);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t launch_prep_x(const PrepBatch& b, bool early_trigger, cudaStream_t stream) {
+    if (b.n < 1 || b.n > kMaxPrepLayers) return cudaErrorInvalidValue;
+    return b.n == 1 ? launch_prep_n<1>(b, early_trigger, stream)
+                    : launch_prep_n<kMaxPrepLayers>(b, early_trigger, stream);
 }
 
 }  // namespace dl

@@ -28,12 +28,32 @@ cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const C
                               const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
                               bool launch);
 
-// FP8 activation prep: x (bf16 [M][K]) -> xh (f16 [KB][2][mtb][64], exact
-// per-block power-of-two scaling, rows >= M zero) and unscale[KB][16];
-// K % 128 == 0.
-// early_trigger: let the main kernel launch before this one's wait (only when
+// FP8 activation prep of up to kMaxPrepLayers layers in one launch: for each,
+// x (bf16 [M][K]) -> xh (f16 [KB][2][mtb][64], exact per-block power-of-two
+// scaling, rows >= M zero) and unscale[KB][16]; K % 128 == 0.
+constexpr int kMaxPrepLayers = 16;
+struct PrepLayer {
+    const uint16_t* x;
+    uint16_t* xh;
+    float* unscale;
+    int M, K, KB, mtb;
+    int pair0;                // set by launch_prep_x: first pair of this layer in the batch
+};
+constexpr int kPrepInFlight = 8;
+template <int NB>
+struct PrepBatchN {
+    PrepLayer layer[NB];
+    int n;
+    int early_trigger;
+    // 1: every layer's x is known ready when the grid starts (no kernel still
+    // running may write it): copy first, then wait for the previous kernel, so
+    // the copy overlaps it while a kernel that waits for this grid still waits
+    // for the previous one too.
+    int wait_last;
+};
+using PrepBatch = PrepBatchN<kMaxPrepLayers>;
+// early_trigger: let the next kernel launch before this one's wait (only when
 // no kernel before it on the stream writes weights or scales).
-cudaError_t launch_prep_x(const uint16_t* x, uint16_t* xh, float* unscale, int M, int K, int KB,
-                          int mtb, bool early_trigger, cudaStream_t stream);
+cudaError_t launch_prep_x(const PrepBatch& b, bool early_trigger, cudaStream_t stream);
 
 }  // namespace dl
