@@ -145,3 +145,30 @@ def test_bf16_first_layer_puts_the_copies_before_it(cuda_device):
             assert torch.equal(got[i], want[i]), (use_graph, i)
     assert dl.device_status() == 0
     dl.graph_cache_clear()
+
+
+def test_one_later_copy_covers_every_block(cuda_device):
+    """Exactly one FP8 layer after layer 0 copied ahead, with more (K block,
+    token slot) pairs (96 x 16) than the copy launch has warps (at most 8 per
+    SM): every block of its copy must be made by this call.  The workspace
+    first serves a list whose layer 1 has the same region but another x, so
+    a block left out would be read stale and give wrong outputs."""
+    M = 4
+    shapes = [(F8, 256, 1024, False), (F8, 256, 12288, True), (F8, 256, 1024, False)]
+    first = independent_layers(cuda_device, shapes, M, 99)
+    second = [first[0], independent_layers(cuda_device, shapes[:2], M, 100)[1]]
+    ws = dl.Workspace.for_stream(first)
+    # layer 0's copy, then layer 1's alone in the launch after layer 0
+    assert dl.decode_stream_launches(second, ws) == 2 + 2
+    st = torch.cuda.Stream()
+    want_first = singles(first, ws)
+    want = singles(second, ws)
+    for use_graph in (False, True):
+        got = run(first, ws, use_graph, st)
+        for i in range(3):
+            assert torch.equal(got[i], want_first[i]), (use_graph, i)
+        got = run(second, ws, use_graph, st)
+        for i in range(2):
+            assert torch.equal(got[i], want[i]), (use_graph, i)
+    assert dl.device_status() == 0
+    dl.graph_cache_clear()

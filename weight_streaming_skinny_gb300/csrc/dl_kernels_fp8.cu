@@ -78,7 +78,8 @@ __device__ __forceinline__ void prep_pair(const PrepLayer& L, int kb, int tok, i
 template <int NB>
 __global__ void __launch_bounds__(256) prep_x_kernel(const __grid_constant__ PrepBatchN<NB> batch) {
     const int lane = threadIdx.x & 31;
-    // (single-layer launches never copy ahead: that code is left out of them)
+    // (copies made ahead always use the batched instance, NB > 1, even for one
+    // layer: that code is left out of the single-layer one)
     if (NB > 1 && batch.wait_last) {
         // x is ready already (see PrepBatch): copy it while the previous
         // kernel runs, then complete only after that kernel has (every thread
@@ -176,8 +177,11 @@ static cudaError_t launch_prep_n(const PrepBatch& b, bool early_trigger, cudaStr
 
 cudaError_t launch_prep_x(const PrepBatch& b, bool early_trigger, cudaStream_t stream) {
     if (b.n < 1 || b.n > kMaxPrepLayers) return cudaErrorInvalidValue;
-    return b.n == 1 ? launch_prep_n<1>(b, early_trigger, stream)
-                    : launch_prep_n<kMaxPrepLayers>(b, early_trigger, stream);
+    // Copies made ahead (wait_last) run only in the batched instance, whatever
+    // the number of layers: the single-layer instance has one warp per pair
+    // and no grid-stride walk, so on the small grid it would leave pairs out.
+    return (b.n == 1 && !b.wait_last) ? launch_prep_n<1>(b, early_trigger, stream)
+                                      : launch_prep_n<kMaxPrepLayers>(b, early_trigger, stream);
 }
 
 }  // namespace dl
