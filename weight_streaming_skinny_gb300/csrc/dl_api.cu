@@ -376,12 +376,19 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
                        const float* scales, const void* bias, void* y, float* y_f32,
                        void* ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo& di,
                        bool after_own, int act, int* idx = nullptr, float* maxval = nullptr,
-                       uint16_t* xh_ready = nullptr, float* unscale_ready = nullptr) {
+                       uint16_t* xh_ready = nullptr, float* unscale_ready = nullptr,
+                       uint16_t* xh_next = nullptr, float* us_next = nullptr,
+                       float* wslot = nullptr) {
     // after_own: every earlier kernel on the stream is one of this library's
     // (a later layer of one dl_decode_stream call), so none writes weights or
     // scales and the next one's weights may be fetched before the wait.
     // xh_ready / unscale_ready (FP8): the activation copy was already written
-    // there by an earlier prep launch of the same stream; no prep here.
+    // there by an earlier launch of the same stream (a prep launch, or the
+    // previous layer's epilogue); no prep here.
+    // xh_next / us_next / wslot: this layer (act 0, N % 128 == 0) also writes
+    // the activation copy of the next layer, an FP8 layer whose x is this y
+    // with the same staged token rows; wslot holds grid x 2 slots of
+    // [mtb][128] fp32 for the tiles that one segment covers whole.
     Plan pl;
     dl_status s = make_plan(dtype, M, N, K, di, pl);
     if (s != DL_OK) return s;
@@ -435,6 +442,12 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.wave_seg0[dl::kMaxWaves] = pl.wave_seg0[pl.n_waves];
     p.stages = pl.stages;
     p.err = di.err_word;
+    p.xh_next = xh_next;
+    p.us_next = us_next;
+    p.wslot = wslot;
+    if (xh_next && (act != 0 || N % dl::kBK != 0 || !us_next || !wslot))
+        return fail(DL_ERR_INVALID_ARG, "internal: next-layer activation copy needs act 0, "
+                    "N %% 128 == 0 and its buffers");
     cudaError_t e;
     if (dtype == DL_BF16) {
         // Inside a stream the previous layer's tail is long: fill the whole ring.
@@ -537,8 +550,15 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // like bf16 layers.  `limit` = the caller's workspace (0: no limit); layers
 // that do not fit get their own prep launch as usual.  off[i] = 0: not
 // hoisted.
+// Then the FP8 layers fed by the layer just before them -- x is exactly that
+// layer's whole y, a plain linear (act 0) with the same M and staged token
+// rows -- get their copy from that layer's epilogue instead of a prep launch
+// (fed[i] = its region, 0: none).  The copies of such layers alternate
+// between two regions, so that a layer never writes the copy it reads; the
+// producing layers share one set of per-CTA slots at `wslot`.
 dl_status plan_stream(const dl_layer* layers, int n, const DeviceInfo& di, size_t limit,
-                      size_t& base, std::vector<size_t>& off, size_t& end) {
+                      size_t& base, std::vector<size_t>& off, size_t& end,
+                      std::vector<size_t>& fed, size_t& wslot) {
     base = 0;
     for (int i = 0; i < n; ++i) {
         Plan pl;
@@ -563,6 +583,37 @@ dl_status plan_stream(const dl_layer* layers, int n, const DeviceInfo& di, size_
         if (limit && end + need > limit) continue;
         off[(size_t)i] = end;
         end += need;
+    }
+    fed.assign((size_t)n, 0);
+    wslot = 0;
+    size_t region = 0, slots = 0;       // the largest copy and the largest slot set
+    std::vector<char> is_fed((size_t)n, 0);
+    for (int i = 1; i < n; ++i) {
+        const dl_layer& L = layers[i];
+        const dl_layer& P = layers[i - 1];
+        if (L.dtype != DL_FP8_B128 || off[(size_t)i] || P.act != 0) continue;
+        if (L.x != P.y || L.M != P.M || L.K != P.N) continue;
+        Plan pl, pp;
+        dl_status s = make_plan(L.dtype, L.M, L.N, L.K, di, pl);
+        if (s == DL_OK) s = make_plan(P.dtype, P.M, P.N, P.K, di, pp);
+        if (s != DL_OK) return s;
+        if (pp.mtb != pl.mtb) continue;
+        const size_t need = align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256) +
+                            align_up((size_t)pl.KB * dl::kUnscaleStride * sizeof(float), 256);
+        const size_t sl = align_up((size_t)pp.grid * 2 * pp.mtb * dl::kBN * sizeof(float), 256);
+        const size_t r = need > region ? need : region, w = sl > slots ? sl : slots;
+        if (limit && end + 2 * r + w > limit) continue;
+        region = r;
+        slots = w;
+        is_fed[(size_t)i] = 1;
+    }
+    if (region) {
+        const size_t r0 = end, r1 = end + region;
+        wslot = end + 2 * region;
+        end = wslot + slots;
+        int k = 0;
+        for (int i = 1; i < n; ++i)
+            if (is_fed[(size_t)i]) fed[(size_t)i] = (k++ & 1) ? r1 : r0;
     }
     return DL_OK;
 }
@@ -710,9 +761,9 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
                         pl.ws_bytes, ws_bytes);
         if ((s = prepare_layer(L.dtype, L.M, L.N, L.K, di)) != DL_OK) return s;
     }
-    size_t base = 0, end = 0;
-    std::vector<size_t> hoist;
-    if ((s = plan_stream(layers, n_layers, di, ws_bytes, base, hoist, end)) != DL_OK) return s;
+    size_t base = 0, end = 0, wslot = 0;
+    std::vector<size_t> hoist, fed;
+    if ((s = plan_stream(layers, n_layers, di, ws_bytes, base, hoist, end, fed, wslot)) != DL_OK) return s;
     char* wsb = static_cast<char*>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto enqueue_all = [&]() -> dl_status {
@@ -724,9 +775,9 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
         // it (wait_last).
         bool any = false;
         auto region = [&](int i, const Plan& pl, uint16_t*& xh, float*& us) {
-            xh = reinterpret_cast<uint16_t*>(wsb + hoist[(size_t)i]);
-            us = reinterpret_cast<float*>(wsb + hoist[(size_t)i] +
-                                          align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256));
+            const size_t o = hoist[(size_t)i] ? hoist[(size_t)i] : fed[(size_t)i];
+            xh = reinterpret_cast<uint16_t*>(wsb + o);
+            us = reinterpret_cast<float*>(wsb + o + align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256));
         };
         auto enqueue_copies = [&](int from, int to, bool wait_last) -> dl_status {
             dl::PrepBatch b{};
@@ -769,11 +820,23 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
             const bool after_own = i > 0 || any;
             uint16_t* xh = nullptr;
             float* us = nullptr;
-            if (hoist[(size_t)i]) {
+            if (hoist[(size_t)i] || fed[(size_t)i]) {
                 Plan pl;
                 dl_status r = make_plan(L.dtype, L.M, L.N, L.K, di, pl);
                 if (r != DL_OK) return r;
                 region(i, pl, xh, us);
+            }
+            // The next layer's copy, when this layer's epilogue makes it.
+            uint16_t* xh_next = nullptr;
+            float* us_next = nullptr;
+            float* slots = nullptr;
+            if (i + 1 < n_layers && fed[(size_t)i + 1]) {
+                const dl_layer& Q = layers[i + 1];
+                Plan pq;
+                dl_status r = make_plan(Q.dtype, Q.M, Q.N, Q.K, di, pq);
+                if (r != DL_OK) return r;
+                region(i + 1, pq, xh_next, us_next);
+                slots = reinterpret_cast<float*>(wsb + wslot);
             }
             // act = 2: y holds the int32 argmax indices; no logits are written.
             dl_status r = L.act == 2
@@ -781,7 +844,8 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
                                workspace, ws_bytes, st, di, after_own, 2, static_cast<int*>(L.y),
                                nullptr, xh, us)
                 : launch_layer(L.dtype, L.M, L.N, L.K, L.x, L.W, L.scales, L.bias, L.y, nullptr,
-                               workspace, ws_bytes, st, di, after_own, L.act, nullptr, nullptr, xh, us);
+                               workspace, ws_bytes, st, di, after_own, L.act, nullptr, nullptr, xh, us,
+                               xh_next, us_next, slots);
             if (r != DL_OK) {
                 std::string m = g_err;
                 return fail(r, "layer %d: %s", i, m.c_str());
@@ -838,9 +902,9 @@ size_t dl_decode_stream_workspace_bytes(const dl_layer* layers, int n_layers) {
         if (validate_layer(layers[i], i) != DL_OK) return 0;
     DeviceInfo di;
     if (device_info(di) != DL_OK) return 0;
-    size_t base = 0, end = 0;
-    std::vector<size_t> hoist;
-    if (plan_stream(layers, n_layers, di, 0, base, hoist, end) != DL_OK) return 0;
+    size_t base = 0, end = 0, wslot = 0;
+    std::vector<size_t> hoist, fed;
+    if (plan_stream(layers, n_layers, di, 0, base, hoist, end, fed, wslot) != DL_OK) return 0;
     return end > base ? end : base;
 }
 
@@ -851,19 +915,21 @@ int dl_decode_stream_launches(const dl_layer* layers, int n_layers, size_t ws_by
         if (validate_layer(layers[i], i) != DL_OK) return -1;
     DeviceInfo di;
     if (device_info(di) != DL_OK) return -1;
-    size_t base = 0, end = 0;
-    std::vector<size_t> hoist;
-    if (plan_stream(layers, n_layers, di, ws_bytes, base, hoist, end) != DL_OK) return -1;
-    int later = 0, fp8 = 0;
+    size_t base = 0, end = 0, wslot = 0;
+    std::vector<size_t> hoist, fed;
+    if (plan_stream(layers, n_layers, di, ws_bytes, base, hoist, end, fed, wslot) != DL_OK) return -1;
+    int later = 0, fp8 = 0, by_epilogue = 0;
     for (int i = 0; i < n_layers; ++i) {
         fp8 += layers[i].dtype == DL_FP8_B128;
         later += i > 0 && hoist[(size_t)i] != 0;
+        by_epilogue += fed[(size_t)i] != 0;
     }
     const int first = hoist[0] != 0;
     // layer 0's copy, the other copies (kMaxPrepLayers per launch), one main
-    // kernel per layer, and a prep kernel before every other FP8 layer
+    // kernel per layer, and a prep kernel before every other FP8 layer whose
+    // copy the layer before does not make
     return first + (later + dl::kMaxPrepLayers - 1) / dl::kMaxPrepLayers + n_layers +
-           (fp8 - first - later);
+           (fp8 - first - later - by_epilogue);
 }
 
 void dl_graph_cache_clear(void) {

@@ -138,6 +138,14 @@ struct LinearParams {
     int early_stages;         // stages whose weights may be fetched before griddepcontrol.wait
                               //   (0: the previous kernel may write weights)
     unsigned* err;            // device error word (bounded waits OR their bit in)
+    // The exact f16 copy of y for a next FP8 layer whose x is this layer's y
+    // (act 0, N % 128 == 0; its copy has the same staged token rows MTB):
+    // xh_next [N/128][2][MTB][64] and us_next [N/128][16], written by the
+    // epilogue of every tile (tile t = K block t of the next layer), or null.
+    uint16_t* xh_next;
+    float* us_next;
+    float* wslot;             // with xh_next: [gridDim.x][2][MTB][kBN] fp32, a CTA's
+                              //   slots for the tiles one segment covers whole
 };
 
 // One pipeline stage holds one unit, or for FP8 up to two consecutive units
@@ -190,7 +198,7 @@ __host__ __device__ constexpr SmemLayout smem_layout(int dtype, int, int mt, int
     L.x = L.w + stages * wbytes;
     L.hdr = L.x + stages * xbytes;
     L.bars = L.hdr + stages * (int)sizeof(StageHeader);
-    L.runs = L.bars + (2 * stages + 4) * 8;
+    L.runs = L.bars + (2 * stages + 5) * 8;
     L.best = L.runs + 2 * (int)sizeof(RunSlot) + 16;      // [8 warps][16 tokens] argmax keys
     L.total = L.best + kConsumerWarps * 16 * 8;
     return L;
@@ -687,6 +695,65 @@ struct ConsumerOf<DT, kMMA, MT> {
     using type = MmaConsumer<DT, MT>;
 };
 
+// ------------------------------------------------------------------ FP8 activation copy
+
+// The exact f16 copy of x for the FP8 path, one (K block kb, token slot tok)
+// pair per warp: lane `lane` holds the bf16 values of columns 4 lane ..
+// 4 lane + 3 of the block in v (zero for tok >= M).  The block is scaled by
+// 2^(141 - e), e the largest biased exponent of its values, so that its
+// largest magnitude lands in [2^14, 2^15); every value is then exact in f16
+// if no non-zero value has a biased exponent below e - 31 (f16 subnormals keep
+// 8 significant bits down to 2^-17) and none is an infinity or NaN.
+// unscale[kb][tok] = 2^(e - 141) (1 for an all-zero block and for the token
+// slots M <= tok < mtb), or 0 when the block is not exact in f16.  xh is
+// [K block][half][mtb token rows][64], rows tok >= M zero; within every group
+// of 16 columns the values sit in the order the FP8 MMA fragments take them
+// (position 2t + j holds column 4t + j and position 2t + 8 + j holds column
+// 4t + 2 + j, t < 4, j < 2), so that a plain ldmatrix of a token row yields
+// the B fragment matching the e4m3 codes 4t .. 4t + 3 a thread holds for the
+// A operand.  The whole warp calls it with the same (kb, tok).
+__device__ __forceinline__ void write_x_copy_pair(uint16_t* __restrict__ xh, float* __restrict__ unscale,
+                                                  int M, int mtb, int kb, int tok, int lane, uint2 v) {
+    // This lane's 4 columns 4t .. 4t + 3 (t = lane % 4) of 16-column group
+    // (lane % 16) / 4 of half lane / 16 go to positions 2t, 2t + 1 and
+    // 2t + 8, 2t + 9 of that group.
+    const long long row = (((long long)kb * 2 + (lane >> 4)) * mtb + tok) * 64 + ((lane & 15) >> 2) * 16;
+    uint16_t* d0 = xh + row + 2 * (lane & 3);
+    uint16_t* d1 = d0 + 8;
+    if (tok >= M) {
+        if (tok < mtb) {
+            *reinterpret_cast<uint32_t*>(d0) = 0u;
+            *reinterpret_cast<uint32_t*>(d1) = 0u;
+        }
+        if (lane == 0) unscale[kb * kUnscaleStride + tok] = 1.f;
+        return;
+    }
+    const uint32_t b[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
+    unsigned emax = 0, emin = 255;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const unsigned mag = b[i] & 0x7fffu;
+        const unsigned e = mag >> 7;
+        emax = e > emax ? e : emax;
+        const unsigned ez = mag ? e : 255u;      // exact zeros do not bound the range
+        emin = ez < emin ? ez : emin;
+        bad |= (e == 255u);
+    }
+    emax = warp_max_u32(emax);
+    emin = warp_min_u32(emin);
+    const bool ok = !__any_sync(0xffffffffu, bad) &&
+                    (emax == 0u || (emax >= 15u && emin + 31u >= emax));
+    const float f = (ok && emax) ? __uint_as_float((268u - emax) << 23) : 0.f;
+    const float x0 = __uint_as_float(v.x << 16) * f, x1 = __uint_as_float(v.x & 0xffff0000u) * f;
+    const float x2 = __uint_as_float(v.y << 16) * f, x3 = __uint_as_float(v.y & 0xffff0000u) * f;
+    *reinterpret_cast<uint32_t*>(d0) = f32x2_to_f16x2(x0, x1);
+    *reinterpret_cast<uint32_t*>(d1) = f32x2_to_f16x2(x2, x3);
+    if (lane == 0)
+        unscale[kb * kUnscaleStride + tok] =
+            !ok ? 0.f : (emax ? __uint_as_float((emax - 14u) << 23) : 1.f);
+}
+
 // ------------------------------------------------------------------ fix-up
 
 // Last arriver of a split tile: y[m][n0 + rr] = the sum, in ascending segment
@@ -697,18 +764,23 @@ struct ConsumerOf<DT, kMMA, MT> {
 // add (float4 rows, up to kBatch segments in flight): one L2 round trip per
 // kBatch segments instead of one per load.  Thread tid owns rows 4 (g % 32) ..
 // + 3 of token g / 32 for g = tid (and tid + 256 when 16 tokens are staged),
-// so a warp's lanes share one token (argmax: one warp reduction per token).
-template <int MTB>
+// so a warp's lanes share one token (argmax: one warp reduction per token;
+// the next layer's activation copy: one block per warp, p.xh_next).
+// kLocal: the tile was covered whole by one segment of this CTA, whose warps
+// stored its rows in the CTA's own slot `local` (no other CTA involved, plain
+// cached loads after a CTA-scope barrier).
+template <int MTB, bool kLocal = false>
 __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int j_first, int j_last,
-                                           int tid, unsigned long long* sbest) {
+                                           int tid, unsigned long long* sbest,
+                                           const float* local = nullptr) {
     constexpr int kBatch = 8;
     constexpr int kG = MTB > 8 ? 2 : 1;                       // row groups per thread
     constexpr long long kStride = 2LL * MTB * kBN;            // floats between segments' slot 0
     const int n0 = tile * kBN;
-    const int sl_first = (seg_begin(p, j_first) / p.UT == tile) ? 0 : 1;
-    const int nseg = j_last - j_first + 1;
+    const int sl_first = kLocal ? 0 : ((seg_begin(p, j_first) / p.UT == tile) ? 0 : 1);
+    const int nseg = kLocal ? 1 : j_last - j_first + 1;
     const int ng = p.M * (kBN / 4);
-    const float* first = p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN;
+    const float* first = kLocal ? local : p.partials + ((long long)j_first * 2 + sl_first) * MTB * kBN;
     int off[kG];
     bool has[kG];
     float4 v[kG];
@@ -726,8 +798,13 @@ __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int 
             const int j = j0 + q;
             const float* src = j == 0 ? first : p.partials + (long long)(j_first + j) * kStride;
 #pragma unroll
-            for (int i = 0; i < kG; ++i)
-                a[i][q] = (has[i] && j < nseg) ? ld_cg_f32x4(src + off[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < kG; ++i) {
+                if (kLocal)
+                    a[i][q] = (has[i] && j < nseg) ? *reinterpret_cast<const float4*>(src + off[i])
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                else
+                    a[i][q] = (has[i] && j < nseg) ? ld_cg_f32x4(src + off[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
@@ -752,15 +829,22 @@ __device__ __forceinline__ void fixup_tile(const LinearParams& p, int tile, int 
         const int m = g >> 5, rr = (g & 31) * 4;
         const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
         unsigned long long k = 0;
+        uint32_t yb[4] = {0u, 0u, 0u, 0u};                   // the bf16 outputs
         if (has[i]) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 if (n0 + rr + c < p.N) {
                     const float vb = write_output(p, m, n0 + rr + c, vv[c]);
+                    yb[c] = f32_to_bf16_rne(vb);
                     if (p.act == 2) k = max_u64(k, argmax_key(vb, n0 + rr + c));
                 }
             }
         }
+        // The next layer's exact f16 copy of this block (K block `tile` of its
+        // x, token m): N % 128 == 0 there, so all 128 columns are outputs.
+        if (p.xh_next)
+            write_x_copy_pair(p.xh_next, p.us_next, p.M, MTB, tile, m, tid & 31,
+                              make_uint2(yb[0] | (yb[1] << 16), yb[2] | (yb[3] << 16)));
         if (p.act == 2 && m < p.M) {                         // the warp's 32 lanes share m
             k = warp_max_key(k, 1);
             if ((tid & 31) == 0) sbest[m] = max_u64(sbest[m], k);
@@ -837,6 +921,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     uint64_t* empty = full + S;
     uint64_t* written = empty + S;    // [2] consumer warps -> ticket warp (count 8)
     uint64_t* result = written + 2;   // [2] ticket warp -> consumer warps (count 1)
+    uint64_t* xch = result + 2;       // consumer warps -> each other (count 8): a whole
+                                      //   tile's rows are in the CTA's slot
     volatile RunSlot* runs = reinterpret_cast<volatile RunSlot*>(smem + L.runs);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.runs + 2 * sizeof(RunSlot));
     // argmax (act = 2): each consumer warp's best key per token
@@ -858,6 +944,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             mbar_init(smem_u32(&written[b]), kConsumerWarps);
             mbar_init(smem_u32(&result[b]), 1);
         }
+        mbar_init(smem_u32(xch), kConsumerWarps);
         *abort_flag = 0;
         fence_mbarrier_init();
         griddep_launch_dependents();
@@ -1070,6 +1157,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     int run_kb0 = 0;
     int n_split = 0;                  // split runs handed to the ticket warp so far
     uint32_t rph = 0u;                // phase parity of result[b] in bit b
+    int n_local = 0;                  // whole tiles finished through the CTA's slots (xh_next)
 
     // Hand split run `tile` (partial rows already stored) to the ticket warp;
     // tile < 0 tells it that there are no more.
@@ -1133,6 +1221,27 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         if (flags & kRunLast) {
             // This run of `tile` is complete: store its rows (y, or the slot).
             const bool whole = (run_kb0 == 0) && (kb + nkb == KB);
+            if (whole && p.xh_next) {
+                // The next layer's activation copy is made from whole blocks
+                // (one warp per token): the warps put the tile's rows in one of
+                // the CTA's two slots, meet, and finish it like a split tile of
+                // one segment.  The slots alternate; a warp reaches the meeting
+                // of a tile only after finishing the tile before, so a slot is
+                // never overwritten while it is read.
+                float* slot = p.wslot + ((long long)blockIdx.x * 2 + (n_local & 1)) * MTB * kBN;
+                c.write_rows(p, slot, tile * kBN, warp, lane, sbest);
+                c.reset();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(xch));
+                if (!mbar_wait_bounded(smem_u32(xch), (uint32_t)(n_local & 1), err, kErrRunWait)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                fixup_tile<MTB, true>(p, tile, 0, 0, threadIdx.x, sbest, slot);
+                ++n_local;
+                if (++s == S) { s = 0; ph ^= 1u; }
+                continue;
+            }
             float* slot = nullptr;
             if (!whole) {
                 const long long first_tile = seg_begin(p, seg) / UT;

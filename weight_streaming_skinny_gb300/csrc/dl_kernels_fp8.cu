@@ -32,47 +32,7 @@ __device__ __forceinline__ uint2 load_pair(const PrepLayer& L, int kb, int tok, 
 
 // One pair: this warp's (K block, token slot) of layer L, from its values v.
 __device__ __forceinline__ void prep_pair(const PrepLayer& L, int kb, int tok, int lane, uint2 v) {
-    uint16_t* __restrict__ xh = L.xh;
-    float* __restrict__ unscale = L.unscale;
-    const int M = L.M, mtb = L.mtb;
-    // This lane's 4 columns 4t .. 4t + 3 (t = lane % 4) of 16-column group
-    // (lane % 16) / 4 of half lane / 16 go to positions 2t, 2t + 1 and
-    // 2t + 8, 2t + 9 of that group.
-    const long long row = (((long long)kb * 2 + (lane >> 4)) * mtb + tok) * 64 + ((lane & 15) >> 2) * 16;
-    uint16_t* d0 = xh + row + 2 * (lane & 3);
-    uint16_t* d1 = d0 + 8;
-    if (tok >= M) {
-        if (tok < mtb) {
-            *reinterpret_cast<uint32_t*>(d0) = 0u;
-            *reinterpret_cast<uint32_t*>(d1) = 0u;
-        }
-        if (lane == 0) unscale[kb * kUnscaleStride + tok] = 1.f;
-        return;
-    }
-    const uint32_t b[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
-    unsigned emax = 0, emin = 255;
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const unsigned mag = b[i] & 0x7fffu;
-        const unsigned e = mag >> 7;
-        emax = e > emax ? e : emax;
-        const unsigned ez = mag ? e : 255u;      // exact zeros do not bound the range
-        emin = ez < emin ? ez : emin;
-        bad |= (e == 255u);
-    }
-    emax = warp_max_u32(emax);
-    emin = warp_min_u32(emin);
-    const bool ok = !__any_sync(0xffffffffu, bad) &&
-                    (emax == 0u || (emax >= 15u && emin + 31u >= emax));
-    const float f = (ok && emax) ? __uint_as_float((268u - emax) << 23) : 0.f;
-    const float x0 = __uint_as_float(v.x << 16) * f, x1 = __uint_as_float(v.x & 0xffff0000u) * f;
-    const float x2 = __uint_as_float(v.y << 16) * f, x3 = __uint_as_float(v.y & 0xffff0000u) * f;
-    *reinterpret_cast<uint32_t*>(d0) = f32x2_to_f16x2(x0, x1);
-    *reinterpret_cast<uint32_t*>(d1) = f32x2_to_f16x2(x2, x3);
-    if (lane == 0)
-        unscale[kb * kUnscaleStride + tok] =
-            !ok ? 0.f : (emax ? __uint_as_float((emax - 14u) << 23) : 1.f);
+    write_x_copy_pair(L.xh, L.unscale, L.M, L.mtb, kb, tok, lane, v);
 }
 
 template <int NB>
