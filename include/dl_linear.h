@@ -240,16 +240,21 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
                            size_t ws_bytes, void* stream, int use_graph);
 
 /*
- * Workspace bytes for which dl_decode_stream makes ahead the activation
- * copies of every FP8 layer among the first 16 whose x no earlier layer of
- * the list writes (no byte of its x lies in an earlier layer's y): layer 0's
- * just before it, the others in a launch that runs alongside layer 0 (or, if
- * layer 0 is not such a layer, before it), so that those layers follow one
- * another without a prep kernel in between: the largest layer's
- * dl_workspace_bytes plus one region per such layer.  With a
- * smaller workspace (at least the largest layer's) the call is still correct;
- * layers whose copy does not fit are prepared one by one.  0 if the list is
- * invalid.  Host-only apart from reading device attributes.
+ * Workspace bytes with which dl_decode_stream makes every FP8 layer's exact
+ * f16 activation copy without a prep launch of its own where it can:
+ *  - made ahead: an FP8 layer among the first 16 whose x no earlier layer of
+ *    the list writes (no byte of its x lies in an earlier layer's y): layer
+ *    0's copy just before it, the others in a launch that runs alongside
+ *    layer 0 (or, if layer 0 is not such a layer, before it); one region per
+ *    such layer;
+ *  - made by the layer before: an FP8 layer whose x is exactly the whole y of
+ *    the layer just before it, a plain linear (act 0) with the same M (and so
+ *    N % 128 == 0): that layer's epilogue writes the copy next to y; two
+ *    alternating regions and per-CTA slots for those producers.
+ * Plus the largest layer's dl_workspace_bytes.  With a smaller workspace (at
+ * least the largest layer's) the call is still correct, with the same
+ * results bit for bit: layers whose copy does not fit get a prep launch.  0
+ * if the list is invalid.  Host-only apart from reading device attributes.
  */
 size_t dl_decode_stream_workspace_bytes(const dl_layer* layers, int n_layers);
 

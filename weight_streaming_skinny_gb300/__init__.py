@@ -428,8 +428,10 @@ def decode_stream(layers, workspace: Workspace, *, use_graph: bool = False, stre
 
 
 def decode_stream_workspace_bytes(layers) -> int:
-    """Workspace bytes for decode_stream over `layers` with every FP8 layer whose
-    x is ready at the start prepared in one launch (see dl_linear.h)."""
+    """Workspace bytes for decode_stream over `layers` with the FP8 activation
+    copies made without per-layer prep launches where possible: ahead for the
+    layers whose x is ready at the start, by the layer before for a layer fed
+    by a plain linear's whole y (see dl_linear.h)."""
     arr = (_Layer * max(1, len(layers)))(*[_layer_struct(L) for L in layers])
     dev = layers[0].x.device if layers else torch.device("cuda", torch.cuda.current_device())
     with torch.cuda.device(dev):
