@@ -237,7 +237,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dl.load()
-    dl.set_override({"auto": 0, "simt": 1, "mma": 2}[args.kernel], 0, 0)
+    dl.set_override({"auto": 0, "simt": 1, "mma": 2, "tc": 3}[args.kernel], 0, 0)
     workload = args.workload
     layers = build_layers(workload, dev)
     ys = [out_buffer(L, dev) for _, L in layers]
@@ -490,7 +490,7 @@ def main():
     ap.add_argument("--mode", choices=["graph", "stream", "calls"], default="graph",
                     help="graph: one dl_decode_stream CUDA-graph replay per step (default); "
                          "stream: dl_decode_stream without a graph; calls: one API call per layer")
-    ap.add_argument("--kernel", choices=["auto", "simt", "mma"], default="auto",
+    ap.add_argument("--kernel", choices=["auto", "simt", "mma", "tc"], default="auto",
                     help="force a kernel family (default: the library's automatic choice)")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the end-to-end leg")
     ap.add_argument("--skip-cpu-baseline", action="store_true", help="omit the oracle timing leg")

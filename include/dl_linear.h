@@ -86,7 +86,13 @@ typedef enum dl_kernel {
     DL_KERNEL_AUTO = 0,
     DL_KERNEL_SIMT = 1,   /* CUDA-core FMA, one weight row per lane (FP8: M <= 2;
                              larger M runs the MMA family)                    */
-    DL_KERNEL_MMA = 2     /* warp-level bf16 tensor-core MMA (mma.sync)        */
+    DL_KERNEL_MMA = 2,    /* warp-level tensor-core MMA (mma.sync): bf16, or f16
+                             for FP8 weights against an exact f16 copy of x    */
+    DL_KERNEL_TC = 3      /* FP8 weights only (bf16 layers keep their automatic
+                             family): 5th-generation tensor cores, tcgen05.mma
+                             kind::f8f6f4 with the e4m3 weight tile read from
+                             shared memory as is, x split exactly into three
+                             e4m3 parts, fp32 accumulators in tensor memory   */
 } dl_kernel;
 
 /*

@@ -80,7 +80,7 @@ def test_workspace_bytes_zero_for_invalid_shapes():
 
 def test_override_validation():
     lib = dl.load()
-    assert lib.dl_set_override(3, 0, 0) == 1
+    assert lib.dl_set_override(4, 0, 0) == 1
     assert lib.dl_set_override(0, 3, 0) == 1
     assert lib.dl_set_override(0, 0, -1) == 1
     assert lib.dl_set_override(0, 0, 0) == 0

@@ -19,7 +19,7 @@ from parity_util import assert_parity, oracle_for, run_gpu, sample_rows
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-FAMILIES = [dl.KERNEL_SIMT, dl.KERNEL_MMA]
+FAMILIES = [dl.KERNEL_SIMT, dl.KERNEL_MMA, dl.KERNEL_TC]   # TC: FP8 only (bf16 runs its auto family)
 
 
 @pytest.fixture(autouse=True)

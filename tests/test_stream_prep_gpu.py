@@ -174,3 +174,40 @@ def test_one_later_copy_covers_every_block(cuda_device):
             assert torch.equal(got[i], want[i]), (use_graph, i)
     assert dl.device_status() == 0
     dl.graph_cache_clear()
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_tensor_memory_family_stream_matches_single_calls(cuda_device, M):
+    """The tensor-memory family (forced): copies made ahead, and the prep
+    launches of layers fed by an earlier layer, write its e4m3 activation
+    parts; the stream equals single calls bit for bit."""
+    specs = [(F8, 1024, 2048, True), (BF, 768, 1024, False), (F8, 512, 4096, False),
+             (F8, 2048, 1024, True)]
+    layers = independent_layers(cuda_device, specs, M, 101)
+    L4 = inputs.make_layer(F8, M, 256, 512, bias=False, config_id=101, layer_idx=4).to(cuda_device)
+    y4 = torch.empty((M, 256), dtype=torch.bfloat16, device=cuda_device)
+    layers.append(dl.Layer(dl.FP8_B128, layers[2].y, L4.w, y4, L4.scales))    # x = y of layer 2
+    dl.set_override(dl.KERNEL_TC, 0, 0)
+    try:
+        ws = dl.Workspace.for_stream(layers)
+        # layer 0's copy, layers 2 and 3 after it, layer 4 (x = y of layer 2) with its own prep
+        assert dl.decode_stream_launches(layers, ws) == 2 + 5 + 1
+        want = []
+        for i, L in enumerate(layers):
+            x = want[2] if i == 4 else L.x
+            y = torch.empty_like(L.y)
+            if L.dtype == dl.BF16:
+                dl.linear_bf16(x, L.w, L.bias, out=y, workspace=ws)
+            else:
+                dl.linear_fp8_block128(x, L.w, L.scales, L.bias, out=y, workspace=ws)
+            want.append(y)
+        torch.cuda.synchronize()
+        st = torch.cuda.Stream()
+        for use_graph in (False, True):
+            got = run(layers, ws, use_graph, st)
+            for i in range(len(layers)):
+                assert torch.equal(got[i], want[i]), (use_graph, i)
+    finally:
+        dl.set_override(0, 0, 0)
+        dl.graph_cache_clear()
+    assert dl.device_status() == 0

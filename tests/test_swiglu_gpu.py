@@ -19,7 +19,7 @@ from parity_util import ABS_TOL, REL_TOL, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-FAMILIES = [dl.KERNEL_SIMT, dl.KERNEL_MMA]
+FAMILIES = [dl.KERNEL_SIMT, dl.KERNEL_MMA, dl.KERNEL_TC]   # TC: FP8 only (bf16 runs its auto family)
 
 
 def swiglu_bound(g, u, ag, au):

@@ -30,7 +30,7 @@ __all__ = [
 
 BF16 = 0
 FP8_B128 = 1
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA = 0, 1, 2
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libdecode_linear.so")

@@ -121,6 +121,7 @@ struct Plan {
     int stages;
     size_t smem;
     size_t counter_off, tickets_off, partials_off, xh_off, unscale_off, ws_bytes;
+    size_t xcopy_bytes;       // FP8: the activation copy (f16, or the tensor-memory family's parts)
 };
 
 int auto_family(int dtype, int M) {
@@ -153,12 +154,14 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     pl.dtype = dtype;
     const int ko = g_kernel_override.load();
     pl.family = ko ? ko : auto_family(dtype, M);
-    if (pl.family != dl::kSIMT && pl.family != dl::kMMA)
+    if (pl.family != dl::kSIMT && pl.family != dl::kMMA && pl.family != dl::kTC)
         return fail(DL_ERR_INVALID_ARG, "kernel override %d unknown", pl.family);
+    // The tensor-memory family multiplies e4m3 by e4m3: FP8 weights only.
+    if (pl.family == dl::kTC && dtype != DL_FP8_B128) pl.family = auto_family(dtype, M);
     // The CUDA-core family decodes FP8 for at most 2 tokens; beyond, the
     // decode cost per code is the same and only the MMA amortises the FMAs.
     if (pl.family == dl::kSIMT && dtype == DL_FP8_B128 && M > 2) pl.family = dl::kMMA;
-    pl.mt = pl.family == dl::kMMA ? (M <= 8 ? 8 : 16) : pow2_at_least(M);
+    pl.mt = pl.family != dl::kSIMT ? (M <= 8 ? 8 : 16) : pow2_at_least(M);
     pl.mtb = dl::host_x_rows(pl.mt);
     pl.KB = (K + dl::kBK - 1) / dl::kBK;
     pl.n_tiles = (N + dl::kBN - 1) / dl::kBN;
@@ -276,9 +279,11 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     pl.partials_off = DL_WORKSPACE_ZERO_BYTES;
     size_t end = pl.partials_off + (size_t)pl.n_segments * 2 * pl.mtb * dl::kBN * sizeof(float);
     pl.xh_off = pl.unscale_off = 0;
+    pl.xcopy_bytes = pl.family == dl::kTC ? (size_t)pl.KB * 3 * pl.mtb * 128
+                                          : (size_t)pl.KB * 2 * pl.mtb * 64 * 2;
     if (dtype == DL_FP8_B128) {
         pl.xh_off = align_up(end, 256);
-        pl.unscale_off = align_up(pl.xh_off + (size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256);
+        pl.unscale_off = align_up(pl.xh_off + pl.xcopy_bytes, 256);
         end = pl.unscale_off + (size_t)pl.KB * dl::kUnscaleStride * sizeof(float);
     }
     pl.ws_bytes = end;
@@ -337,6 +342,15 @@ dl_status encode_maps(const Plan& pl, int M, int N, int K, const void* x, const 
         const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
         const cuuint32_t box[2] = {64, (cuuint32_t)pl.mtb};
         r = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
+                ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (pl.family == dl::kTC) {
+        // The tensor-memory family's e4m3 parts: rows of 128 bytes, [K block]
+        // [part][mtb]; one box = the 6 mtb rows of two consecutive K blocks.
+        const cuuint64_t dims[2] = {128, (cuuint64_t)pl.KB * 3 * pl.mtb};
+        const cuuint64_t strides[1] = {128};
+        const cuuint32_t box[2] = {128, (cuuint32_t)(6 * pl.mtb)};
+        r = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(x), dims, strides, box,
                 ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
@@ -465,7 +479,8 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
         if (e == cudaSuccess && !prepped) {
             dl::PrepBatch b{};
             b.n = 1;
-            b.layer[0] = dl::PrepLayer{static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, pl.mtb, 0};
+            b.layer[0] = dl::PrepLayer{static_cast<const uint16_t*>(x), xh, unscale, M, K, pl.KB, pl.mtb, 0,
+                                       pl.family == dl::kTC ? 1 : 0};
             e = dl::launch_prep_x(b, after_own, stream);
         }
         if (e == cudaSuccess)
@@ -578,7 +593,7 @@ dl_status plan_stream(const dl_layer* layers, int n, const DeviceInfo& di, size_
         Plan pl;
         dl_status s = make_plan(L.dtype, L.M, L.N, L.K, di, pl);
         if (s != DL_OK) return s;
-        const size_t need = align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256) +
+        const size_t need = align_up(pl.xcopy_bytes, 256) +
                             align_up((size_t)pl.KB * dl::kUnscaleStride * sizeof(float), 256);
         if (limit && end + need > limit) continue;
         off[(size_t)i] = end;
@@ -597,8 +612,9 @@ dl_status plan_stream(const dl_layer* layers, int n, const DeviceInfo& di, size_
         dl_status s = make_plan(L.dtype, L.M, L.N, L.K, di, pl);
         if (s == DL_OK) s = make_plan(P.dtype, P.M, P.N, P.K, di, pp);
         if (s != DL_OK) return s;
-        if (pp.mtb != pl.mtb) continue;
-        const size_t need = align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256) +
+        // the epilogue writes the f16 copy (not the tensor-memory family's parts)
+        if (pp.mtb != pl.mtb || pl.family == dl::kTC) continue;
+        const size_t need = align_up(pl.xcopy_bytes, 256) +
                             align_up((size_t)pl.KB * dl::kUnscaleStride * sizeof(float), 256);
         const size_t sl = align_up((size_t)pp.grid * 2 * pp.mtb * dl::kBN * sizeof(float), 256);
         const size_t r = need > region ? need : region, w = sl > slots ? sl : slots;
@@ -632,7 +648,7 @@ int dl_version(void) { return DL_VERSION; }
 const char* dl_last_error(void) { return g_err; }
 
 dl_status dl_set_override(int kernel, int ctas_per_sm, int max_ctas) {
-    if (kernel < 0 || kernel > 2) return fail(DL_ERR_INVALID_ARG, "kernel override %d unknown", kernel);
+    if (kernel < 0 || kernel > 3) return fail(DL_ERR_INVALID_ARG, "kernel override %d unknown", kernel);
     if (ctas_per_sm < 0 || ctas_per_sm > 2)
         return fail(DL_ERR_INVALID_ARG, "ctas_per_sm must be 0, 1 or 2");
     if (max_ctas < 0) return fail(DL_ERR_INVALID_ARG, "max_ctas must be >= 0");
@@ -777,7 +793,7 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
         auto region = [&](int i, const Plan& pl, uint16_t*& xh, float*& us) {
             const size_t o = hoist[(size_t)i] ? hoist[(size_t)i] : fed[(size_t)i];
             xh = reinterpret_cast<uint16_t*>(wsb + o);
-            us = reinterpret_cast<float*>(wsb + o + align_up((size_t)pl.KB * 2 * pl.mtb * 64 * 2, 256));
+            us = reinterpret_cast<float*>(wsb + o + align_up(pl.xcopy_bytes, 256));
         };
         auto enqueue_copies = [&](int from, int to, bool wait_last) -> dl_status {
             dl::PrepBatch b{};
@@ -791,7 +807,8 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
                 uint16_t* xh;
                 float* us;
                 region(i, pl, xh, us);
-                b.layer[b.n++] = dl::PrepLayer{static_cast<const uint16_t*>(L.x), xh, us, L.M, L.K, pl.KB, pl.mtb, 0};
+                b.layer[b.n++] = dl::PrepLayer{static_cast<const uint16_t*>(L.x), xh, us, L.M, L.K, pl.KB,
+                                               pl.mtb, 0, pl.family == dl::kTC ? 1 : 0};
                 if (b.n == dl::kMaxPrepLayers || i == to - 1) {
                     const cudaError_t e = dl::launch_prep_x(b, false, st);
                     if (e != cudaSuccess) return fail(DL_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));

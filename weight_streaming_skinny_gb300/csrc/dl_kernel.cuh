@@ -90,6 +90,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kLoaderWarp = kConsumerWarps;       // warp 8: TMA producer
 constexpr int kTicketWarp = kConsumerWarps + 1;   // warp 9: split-K arrival tickets
+constexpr int kMmaWarp = kConsumerWarps + 2;      // warp 10 (tensor-memory family): MMA issue
 constexpr int kThreads = kConsumerThreads + 64;
 constexpr int kMaxWaves = 24;
 constexpr int kUnscaleStride = 16;       // unscale factors per k-block (one per token slot)
@@ -99,7 +100,18 @@ constexpr int kUnscaleStride = 16;       // unscale factors per k-block (one per
 constexpr int kClaimDepth = 3;
 
 enum DType { kBF16 = 0, kFP8 = 1 };
-enum Family { kSIMT = 1, kMMA = 2 };
+enum Family { kSIMT = 1, kMMA = 2, kTC = 3 };
+
+// Tensor-memory family (FP8 only): B-operand rows per K block (3 activation
+// parts x the token slots), the MMA's N (a multiple of 16; MT = 8 reads 8
+// rows past a unit's 24, whose columns are ignored), and TMEM columns: two
+// buffers of two units.
+template <int MT>
+struct TcShape {
+    static constexpr int rows = 3 * MT;
+    static constexpr int n = rows < 32 ? 32 : rows;
+    static constexpr int cols = 2 * 2 * n <= 128 ? 128 : 256;
+};
 
 // Stage header flags.
 constexpr int kRunFirst = 1;   // first unit of a run (a run = one tile inside one segment)
@@ -189,23 +201,29 @@ struct RunSlot {
     int last;                 // ticket result: tile if this run completed it, else -1
 };
 
-__host__ __device__ constexpr SmemLayout smem_layout(int dtype, int, int mt, int stages) {
+__host__ __device__ constexpr SmemLayout smem_layout(int dtype, int family, int mt, int stages) {
     const int mtb = mt < 8 ? 8 : mt;
     const int wbytes = kStageWBytes;
-    const int xbytes = mtb * kBK * 2 * (dtype == kBF16 ? 1 : kMaxUnitsPerStage);
+    const int xbytes = family == kTC ? kMaxUnitsPerStage * 3 * mtb * 128
+                                     : mtb * kBK * 2 * (dtype == kBF16 ? 1 : kMaxUnitsPerStage);
     SmemLayout L{};
     L.w = 0;
     L.x = L.w + stages * wbytes;
     L.hdr = L.x + stages * xbytes;
     L.bars = L.hdr + stages * (int)sizeof(StageHeader);
-    L.runs = L.bars + (2 * stages + 5) * 8;
+    // full[S], empty[S], written[2], result[2], xch, mma_done[2], tmem_free[2],
+    // the TMEM address (8 bytes)
+    L.runs = L.bars + (2 * stages + 10) * 8;
     L.best = L.runs + 2 * (int)sizeof(RunSlot) + 16;      // [8 warps][16 tokens] argmax keys
     L.total = L.best + kConsumerWarps * 16 * 8;
     return L;
 }
 
-// Threads of a CTA: 8 consumer warps, the loader warp and the ticket warp.
-__host__ __device__ constexpr int threads_for(int, int) { return kThreads; }
+// Threads of a CTA: 8 consumer warps, the loader warp and the ticket warp
+// (and the MMA-issue warp of the tensor-memory family).
+__host__ __device__ constexpr int threads_for(int, int family) {
+    return family == kTC ? kThreads + 32 : kThreads;
+}
 
 // CTAs per SM an instance is compiled for: one, with the whole register file
 // and shared memory of the SM.  (A grid of two CTAs per SM can still be asked
@@ -686,9 +704,114 @@ struct MmaConsumer {
     }
 };
 
+// Tensor-memory consumer (FP8, kind::f8f6f4 MMAs issued by the MMA warp).
+// The MMA of a unit leaves D[row][n] in TMEM, row = weight row of the tile
+// (TMEM lane), column n = part * MT + token slot.  Warps 0-3 each read the
+// 32 lanes of their TMEM quadrant, so thread (w, l) owns weight row 32 w + l
+// and acc[m] is its sum for token m; warps 4-7 hold nothing.
+template <int MT>
+struct TcConsumer {
+    static_assert(MT == 8 || MT == 16, "tensor-memory consumer stages 8 or 16 tokens");
+    float acc[MT];
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    }
+
+    // Add one unit's D (columns at taddr) times the unscale factors and the
+    // block scale: value = (d0 + d1 2^-4) + d2 2^-8 for the three parts.
+    __device__ __forceinline__ void add_tmem_unit(uint32_t taddr, const float (&u)[MT], float scale) {
+        constexpr int C = TcShape<MT>::rows;          // 24 or 48 columns used
+        float d[C + (C % 16 ? 16 - C % 16 : 0)];
+#pragma unroll
+        for (int c = 0; c < C; c += 16) {
+            float v[16];
+            tmem_ld16(taddr + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) d[c + i] = v[i];
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const float v = fmaf(d[2 * MT + m], 0.00390625f, fmaf(d[MT + m], 0.0625f, d[m]));
+            acc[m] = fmaf(v * u[m], scale, acc[m]);
+        }
+    }
+
+    // One unit from the bf16 x in global memory with the exact e4m3 -> bf16
+    // decode (NaN codes stay NaN), for a unit whose activations the parts do
+    // not hold exactly: row `row` of the 128B-swizzled weight tile at sw.
+    __device__ __forceinline__ void add_exact_unit(uint32_t sw, const LinearParams& p, int kb, int row,
+                                                   float scale) {
+        const uint16_t* xk = p.x + (long long)kb * kBK;
+        float part[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[m] = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+            const uint4 w = lds128(sw + row * 128 + ((c ^ (row & 7)) << 4));
+            const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
+            uint32_t wb[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                wb[2 * i] = e4m3x2_to_bf16x2(wq[i] & 0xffffu);
+                wb[2 * i + 1] = e4m3x2_to_bf16x2(wq[i] >> 16);
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m >= p.M) continue;
+                const uint16_t* xm = xk + (long long)m * p.K + 16 * c;
+                const uint4 x0 = ldg128(xm), x1 = ldg128(xm + 8);
+                float a = part[m];
+                a = fma2_bf16(wb[0], x0.x, a);
+                a = fma2_bf16(wb[1], x0.y, a);
+                a = fma2_bf16(wb[2], x0.z, a);
+                a = fma2_bf16(wb[3], x0.w, a);
+                a = fma2_bf16(wb[4], x1.x, a);
+                a = fma2_bf16(wb[5], x1.y, a);
+                a = fma2_bf16(wb[6], x1.z, a);
+                a = fma2_bf16(wb[7], x1.w, a);
+                part[m] = a;
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = fmaf(part[m], scale, acc[m]);
+    }
+
+    // Finish a run: thread (w < 4, l) stores weight row 32 w + l for every
+    // token (SwiGLU on a finished tile: gate row l < 8 of each 16-row group
+    // pairs with up row l + 8, lane l ^ 8; argmax: the warp's best per token
+    // goes to its row sbest[16]).
+    __device__ __forceinline__ void write_rows(const LinearParams& p, float* slot, int n0, int warp,
+                                               int lane, unsigned long long* sbest) {
+        if (warp >= 4) return;
+        const int row = warp * 32 + lane;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const float v = acc[m];
+            if (p.act == 1 && !slot) {
+                const float up = __shfl_xor_sync(0xffffffffu, v, 8);
+                if ((lane & 8) == 0 && m < p.M && n0 + row < p.N) write_swiglu(p, m, n0 + row, v, up);
+            } else if (p.act == 2 && !slot) {
+                unsigned long long k = 0;
+                if (m < p.M && n0 + row < p.N) k = argmax_key(write_output(p, m, n0 + row, v), n0 + row);
+                k = warp_max_key(k, 1);
+                if (lane == 0 && m < p.M) sbest[m] = max_u64(sbest[m], k);
+            } else {
+                put_value(p, slot, n0, m, row, v);
+            }
+        }
+    }
+};
+
 template <int DT, int FAM, int MT>
 struct ConsumerOf {
     using type = SimtConsumer<DT, MT>;
+};
+template <int DT, int MT>
+struct ConsumerOf<DT, kTC, MT> {
+    using type = TcConsumer<MT>;
 };
 template <int DT, int MT>
 struct ConsumerOf<DT, kMMA, MT> {
@@ -752,6 +875,80 @@ __device__ __forceinline__ void write_x_copy_pair(uint16_t* __restrict__ xh, flo
     if (lane == 0)
         unscale[kb * kUnscaleStride + tok] =
             !ok ? 0.f : (emax ? __uint_as_float((emax - 14u) << 23) : 1.f);
+}
+
+// The tensor-memory family's copy of x: three e4m3 parts per value, so that
+// the 5th-generation tensor cores multiply e4m3 weights by e4m3 activations
+// (kind::f8f6f4) with every product exact.  Per (K block kb, token slot tok),
+// with e the largest biased exponent of the block's bf16 values, x is scaled
+// by f = 2^(134 - e) (its largest magnitude lands in [2^7, 2^8)) and split:
+// p0 = e4m3(x f), p1 = e4m3((x f - p0) 2^4), p2 = e4m3(((x f - p0) 2^4 - p1) 2^4),
+// each rounded to nearest even.  x f = p0 + p1 2^-4 + p2 2^-8 exactly when the
+// last remainder is zero: every non-zero value within about 17 binades of
+// the block's largest.  unscale[kb][tok] = 2^(e - 134) (1 for an all-zero
+// block and for the token slots M <= tok < mtb), or 0 when the split is not
+// exact (the block then takes the exact bf16 route).  Layout: rows of 128
+// bytes, [K block][part][mtb token slots], rows tok >= M zero; byte k of a
+// row is column k of the block, so a SWIZZLE_128B tensor copy of rows lands
+// as the K-major B operand of the MMA.  Lane `lane` holds columns 4 lane ..
+// 4 lane + 3 of the block in v; the whole warp calls it with the same (kb, tok).
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h2, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+}
+
+__device__ __forceinline__ void e4m3x4_to_f32x4(uint32_t four, float (&v)[4]) {
+    uint32_t lo, hi;
+    e4m3x4_to_f16x2x2(four, lo, hi);
+    f16x2_to_f32x2(lo, v[0], v[1]);
+    f16x2_to_f32x2(hi, v[2], v[3]);
+}
+
+__device__ __forceinline__ void write_x_parts_pair(uint8_t* __restrict__ xp, float* __restrict__ unscale,
+                                                   int M, int mtb, int kb, int tok, int lane, uint2 v) {
+    uint8_t* row0 = xp + ((long long)kb * 3 * mtb + tok) * 128 + 4 * lane;
+    const long long part = (long long)mtb * 128;           // bytes between the parts' rows
+    if (tok >= M) {
+        if (tok < mtb) {
+#pragma unroll
+            for (int q = 0; q < 3; ++q) *reinterpret_cast<uint32_t*>(row0 + q * part) = 0u;
+        }
+        if (lane == 0) unscale[kb * kUnscaleStride + tok] = 1.f;
+        return;
+    }
+    const uint32_t b[4] = {v.x & 0xffffu, v.x >> 16, v.y & 0xffffu, v.y >> 16};
+    unsigned emax = 0;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const unsigned e = (b[i] & 0x7fffu) >> 7;
+        emax = e > emax ? e : emax;
+        bad |= (e == 255u);
+    }
+    emax = warp_max_u32(emax);
+    bad = __any_sync(0xffffffffu, bad) || (emax != 0u && emax < 8u);
+    // 2^(134 - e) as an fp32 bit pattern (0 for an all-zero or unusable block)
+    const float f = (!bad && emax) ? __uint_as_float((261u - emax) << 23) : 0.f;
+    float x[4], r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = __uint_as_float(b[i] << 16) * f;
+    uint32_t q[3];
+    bool rest = false;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        q[k] = f32x2_to_e4m3x2(x[0], x[1]) | (f32x2_to_e4m3x2(x[2], x[3]) << 16);
+        e4m3x4_to_f32x4(q[k], r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = (x[i] - r[i]) * 16.f;      // exact
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rest |= (x[i] != 0.f);
+    const bool ok = !bad && !__any_sync(0xffffffffu, rest);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) *reinterpret_cast<uint32_t*>(row0 + k * part) = q[k];
+    if (lane == 0)
+        unscale[kb * kUnscaleStride + tok] =
+            !ok ? 0.f : (emax ? __uint_as_float((emax - 7u) << 23) : 1.f);
 }
 
 // ------------------------------------------------------------------ fix-up
@@ -906,7 +1103,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     using Consumer = typename ConsumerOf<DT, FAM, MT>::type;
     constexpr int MTB = XRows<MT>::v;
     constexpr int W_UNIT = TileBytes<DT>::w;                 // weights of one unit
-    constexpr int X_UNIT = MTB * kBK * 2;                   // activations of one unit
+    // activations of one unit: bf16 x, the f16 copy, or (tensor-memory
+    // family) the three e4m3 parts of every token slot, 128 bytes per row
+    constexpr int X_UNIT = FAM == kTC ? TcShape<MTB>::rows * 128 : MTB * kBK * 2;
     constexpr int X_STAGE = DT == kBF16 ? X_UNIT : kMaxUnitsPerStage * X_UNIT;
 
     extern __shared__ uint8_t smem_raw[];
@@ -923,6 +1122,9 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     uint64_t* result = written + 2;   // [2] ticket warp -> consumer warps (count 1)
     uint64_t* xch = result + 2;       // consumer warps -> each other (count 8): a whole
                                       //   tile's rows are in the CTA's slot
+    uint64_t* mma_done = xch + 1;     // [2] tensor-memory family: a stage's MMAs completed
+    uint64_t* tmem_free = mma_done + 2;   // [2] warps 0-3 have read a TMEM buffer (count 4)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_free + 2);
     volatile RunSlot* runs = reinterpret_cast<volatile RunSlot*>(smem + L.runs);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.runs + 2 * sizeof(RunSlot));
     // argmax (act = 2): each consumer warp's best key per token
@@ -938,13 +1140,18 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), kConsumerWarps);
+            // tensor-memory family: the stage's MMAs (one commit) read it too
+            mbar_init(smem_u32(&empty[s]), kConsumerWarps + (FAM == kTC ? 1 : 0));
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&written[b]), kConsumerWarps);
             mbar_init(smem_u32(&result[b]), 1);
         }
         mbar_init(smem_u32(xch), kConsumerWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&mma_done[b]), 1);
+            mbar_init(smem_u32(&tmem_free[b]), 4);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
         griddep_launch_dependents();
@@ -953,10 +1160,77 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_x);
     }
+    if constexpr (FAM == kTC) {
+        // The accumulators of two stages (two units each) in tensor memory.
+        // One CTA per SM, so the columns are free; this warp frees them
+        // before the CTA exits, on every path.
+        if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), TcShape<MTB>::cols);
+        tc_fence_before_sync();
+    }
     __syncthreads();
+    if constexpr (FAM == kTC) tc_fence_after_sync();
     // Everyone but the loader sleeps until the previous kernel on the stream
     // has finished (a hardware wait, no polling while it runs).
     if (warp != kLoaderWarp) griddep_wait();
+
+    // ---------------------------------------------------------------- MMA warp
+    // Tensor-memory family: for each stage, in order, one thread issues the
+    // UMMAs of its units (4 K steps of 32 per unit, M = 128 weight rows, N =
+    // the activation parts) into TMEM buffer (stage number & 1), then commits
+    // twice: to mma_done of that buffer (warps 0-3 read the results) and to
+    // the stage's empty barrier (its buffer may be refilled once the MMAs have
+    // read it).  A buffer is reused only after warps 0-3 freed it.
+    if constexpr (FAM == kTC) {
+        if (warp == kMmaWarp) {
+            constexpr int NU = TcShape<MTB>::n;
+            constexpr uint32_t idesc = umma_idesc_e4m3(NU);
+            const uint32_t tmem = *tmem_slot;
+            if (lane == 0) {
+                long long seq = 0;
+                int s = 0;
+                uint32_t ph = 0;
+                while (true) {
+                    if (!mbar_wait_bounded(smem_u32(&full[s]), ph, err, kErrConsumerWait)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    if ((hdr[s].flags & kDone) || *abort_flag) break;
+                    const int nkb = hdr[s].nkb;
+                    const int b = (int)(seq & 1);
+                    if (seq >= 2 && !mbar_wait_bounded(smem_u32(&tmem_free[b]), (uint32_t)(((seq >> 1) - 1) & 1),
+                                                       err, kErrRunWait)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sw = smem_u32(sW + (size_t)s * kStageWBytes);
+                    const uint32_t sx = smem_u32(sX + (size_t)s * X_STAGE);
+                    for (int u = 0; u < nkb; ++u) {
+                        const uint32_t d = tmem + (uint32_t)((b * 2 + u) * NU);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            umma_e4m3(d, umma_desc_sw128(sw + u * W_UNIT + 32 * j),
+                                      umma_desc_sw128(sx + u * X_UNIT + 32 * j), idesc, j > 0);
+                    }
+                    umma_commit(smem_u32(&mma_done[b]));
+                    umma_commit(smem_u32(&empty[s]));
+                    ++seq;
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+                // Free the columns only once the last MMAs have completed and
+                // warps 0-3 have read their results (bounded waits).
+                if (seq >= 1)
+                    mbar_wait_bounded(smem_u32(&mma_done[(seq - 1) & 1]), (uint32_t)(((seq - 1) >> 1) & 1), err,
+                                      kErrDrainWait);
+                for (long long q = seq >= 2 ? seq - 2 : 0; q < seq; ++q)
+                    mbar_wait_bounded(smem_u32(&tmem_free[q & 1]), (uint32_t)((q >> 1) & 1), err, kErrDrainWait);
+            }
+            __syncwarp();
+            tc_fence_after_sync();
+            tmem_dealloc(tmem, TcShape<MTB>::cols);
+            return;
+        }
+    }
 
     // ---------------------------------------------------------------- ticket warp
     // For each split run, in order: wait until all consumer warps have stored
@@ -1015,7 +1289,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 if constexpr (DT == kFP8) {
                     bulk_load(smem_u32(&hdr[s].unscale[0][0]), p.unscale + (long long)kb * kUnscaleStride,
                               (uint32_t)(nkb * kUnscaleStride * 4), bar);
-                    tma_load_2d(dx, &tm_x, bar, 0, kb * 2 * MTB, pol_x);
+                    if constexpr (FAM == kTC)     // the parts of K blocks kb, kb + 1: 2 x 3 MTB rows
+                        tma_load_2d(dx, &tm_x, bar, 0, kb * TcShape<MTB>::rows, pol_x);
+                    else
+                        tma_load_2d(dx, &tm_x, bar, 0, kb * 2 * MTB, pol_x);
                 } else {
                     tma_load_2d(dx, &tm_x, bar, kb * kBK, 0, pol_x);
                     tma_load_2d(dx + MTB * 128, &tm_x, bar, kb * kBK + 64, 0, pol_x);
@@ -1158,6 +1435,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     int n_split = 0;                  // split runs handed to the ticket warp so far
     uint32_t rph = 0u;                // phase parity of result[b] in bit b
     int n_local = 0;                  // whole tiles finished through the CTA's slots (xh_next)
+    long long tc_seq = 0;             // tensor-memory family: stages consumed (TMEM buffer, parities)
+    const uint32_t tmem = FAM == kTC ? *tmem_slot : 0u;
 
     // Hand split run `tile` (partial rows already stored) to the ticket warp;
     // tile < 0 tells it that there are no more.
@@ -1207,16 +1486,59 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const uint32_t sw = smem_u32(sW + (size_t)s * kStageWBytes);
         const uint32_t sx = smem_u32(sX + (size_t)s * X_STAGE);
         int nkb = 1;
-        if constexpr (DT == kFP8) {
+        if constexpr (FAM == kTC) {
+            // Warps 0-3: a unit whose activation parts are not exact (an
+            // unscale factor 0) is computed here from the weight tile, before
+            // the buffer is released; the others are read from TMEM after
+            // the MMA warp's commit, then the TMEM buffer is released.
+            constexpr int NU = TcShape<MTB>::n;
             nkb = hd.nkb;
-            c.consume(sw, sx, hd.scale[0], hd.unscale[0], kb, p, warp, lane);
-            if (nkb == 2)
-                c.consume(sw + W_UNIT, sx + X_UNIT, hd.scale[1], hd.unscale[1], kb + 1, p, warp, lane);
+            float sc[2], u[2][MT];
+            bool fb[2] = {false, false};
+            if (warp < 4) {
+#pragma unroll
+                for (int uu = 0; uu < 2; ++uu) {
+                    sc[uu] = hd.scale[uu];
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        u[uu][m] = hd.unscale[uu][m];
+                        if (uu < nkb && m < p.M) fb[uu] |= (u[uu][m] == 0.f);
+                    }
+                }
+                const int row = warp * 32 + lane;
+                if (fb[0]) c.add_exact_unit(sw, p, kb, row, sc[0]);
+                if (nkb == 2 && fb[1]) c.add_exact_unit(sw + W_UNIT, p, kb + 1, row, sc[1]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            if (warp < 4) {
+                const int b = (int)(tc_seq & 1);
+                if (!mbar_wait_bounded(smem_u32(&mma_done[b]), (uint32_t)((tc_seq >> 1) & 1), err,
+                                       kErrConsumerWait)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t t0 = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 2 * NU);
+                if (!fb[0]) c.add_tmem_unit(t0, u[0], sc[0]);
+                if (nkb == 2 && !fb[1]) c.add_tmem_unit(t0 + NU, u[1], sc[1]);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tmem_free[b]));
+            }
+            ++tc_seq;
         } else {
-            c.consume(sw, sx, 1.f, nullptr, kb, p, warp, lane);
+            if constexpr (DT == kFP8) {
+                nkb = hd.nkb;
+                c.consume(sw, sx, hd.scale[0], hd.unscale[0], kb, p, warp, lane);
+                if (nkb == 2)
+                    c.consume(sw + W_UNIT, sx + X_UNIT, hd.scale[1], hd.unscale[1], kb + 1, p, warp, lane);
+            } else {
+                c.consume(sw, sx, 1.f, nullptr, kb, p, warp, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
 
         if (flags & kRunLast) {
             // This run of `tile` is complete: store its rows (y, or the slot).

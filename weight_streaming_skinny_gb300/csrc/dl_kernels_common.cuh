@@ -56,6 +56,14 @@ cudaError_t launch_family(int family, int mt, const CUtensorMap& tw, const CUten
         if (mt == 16) return launch_instance<DT, kMMA, 16>(tw, tx, p, grid, smem, stream, launch);
         return cudaErrorInvalidValue;
     }
+    if (family == kTC) {
+        // tensor-memory family: FP8 weights only (kind::f8f6f4 MMAs)
+        if constexpr (DT == kFP8) {
+            if (mt == 8) return launch_instance<DT, kTC, 8>(tw, tx, p, grid, smem, stream, launch);
+            if (mt == 16) return launch_instance<DT, kTC, 16>(tw, tx, p, grid, smem, stream, launch);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (mt) {
         case 1: return launch_instance<DT, kSIMT, 1>(tw, tx, p, grid, smem, stream, launch);
         case 2: return launch_instance<DT, kSIMT, 2>(tw, tx, p, grid, smem, stream, launch);

@@ -32,7 +32,10 @@ __device__ __forceinline__ uint2 load_pair(const PrepLayer& L, int kb, int tok, 
 
 // One pair: this warp's (K block, token slot) of layer L, from its values v.
 __device__ __forceinline__ void prep_pair(const PrepLayer& L, int kb, int tok, int lane, uint2 v) {
-    write_x_copy_pair(L.xh, L.unscale, L.M, L.mtb, kb, tok, lane, v);
+    if (L.parts)
+        write_x_parts_pair(reinterpret_cast<uint8_t*>(L.xh), L.unscale, L.M, L.mtb, kb, tok, lane, v);
+    else
+        write_x_copy_pair(L.xh, L.unscale, L.M, L.mtb, kb, tok, lane, v);
 }
 
 template <int NB>

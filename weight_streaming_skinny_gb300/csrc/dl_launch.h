@@ -30,7 +30,8 @@ cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const C
 
 // FP8 activation prep of up to kMaxPrepLayers layers in one launch: for each,
 // x (bf16 [M][K]) -> xh (f16 [KB][2][mtb][64], exact per-block power-of-two
-// scaling, rows >= M zero) and unscale[KB][16]; K % 128 == 0.
+// scaling, rows >= M zero; or, parts = 1, three e4m3 parts [KB][3][mtb][128]
+// for the tensor-memory family) and unscale[KB][16]; K % 128 == 0.
 constexpr int kMaxPrepLayers = 16;
 struct PrepLayer {
     const uint16_t* x;
@@ -38,6 +39,7 @@ struct PrepLayer {
     float* unscale;
     int M, K, KB, mtb;
     int pair0;                // set by launch_prep_x: first pair of this layer in the batch
+    int parts;                // 0: the f16 copy; 1: the e4m3 parts
 };
 constexpr int kPrepInFlight = 8;
 template <int NB>
