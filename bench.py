@@ -228,6 +228,19 @@ def launch(dl, L, y, ws, stream):
         dl.linear_fp8_block128(L.x, L.w, L.scales, L.bias, out=y, workspace=ws, stream=stream)
 
 
+def replica_rate(local_s: float, bytes_per_rank: float, dist, world: int):
+    """Whole-job throughput of `world` independent replicas (weak scaling):
+    the bytes every rank processed over the slowest rank's time.  Returns
+    (seconds, GB/s); with torch.distributed the local time is reduced with MAX
+    over the ranks (gloo, CPU tensors)."""
+    if dist is not None:
+        import torch
+        t = torch.tensor([local_s], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        local_s = float(t.item())
+    return local_s, bytes_per_rank * world / local_s / 1e9
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import weight_streaming_skinny_gb300 as dl
@@ -300,14 +313,9 @@ def run_ours(args, rank, world, dist):
         stream.synchronize()
         extra_steps += 10
     sampler.stop()
-    total_ms = t0.elapsed_time(t1)
-    if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_s, value = replica_rate(t0.elapsed_time(t1) * 1e-3, step_bytes * K, dist, world)
+    total_ms = total_s * 1e3
     ms_per_step = total_ms / K
-    value = step_bytes * world * K / (total_ms * 1e-3) / 1e9
 
     # ---- per-layer breakdown (single calls, events around each kernel; untimed)
     per_layer = {}
@@ -413,12 +421,8 @@ def run_ours(args, rank, world, dist):
             for _ in range(E):
                 e2e_step()
             el = time.perf_counter() - a
-        if dist is not None:
-            import torch.distributed as tdist
-            t = torch.tensor([el], dtype=torch.float64)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            el = float(t.item())
-        e2e = {"value": round(step_bytes * world * E / el / 1e9, 2), "unit": "GB/s",
+        el, e2e_gbs = replica_rate(el, step_bytes * E, dist, world)
+        e2e = {"value": round(e2e_gbs, 2), "unit": "GB/s",
                "ms_per_step": round(el / E * 1e3, 4), "steps": E,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "each step: the inputs copied host->device and the results device->host "
