@@ -5,7 +5,7 @@
 // bf16, or 256 columns (two 128x128 scale blocks) of FP8.  The U = tiles x
 // units-per-tile units, in tile-major order, are cut into
 // contiguous segments by a partition fixed by (M, N, K, SM count) alone: a
-// first wave of one large segment per CTA (about 5/8 of the work), then waves
+// first wave of one large segment per CTA (about 7/8 of the work), then waves
 // of segments that halve in size down to a small minimum.  A persistent grid
 // of about one CTA per SM takes segment blockIdx.x of the first wave and then
 // claims further segments, in order, from an atomic counter, so SMs that
@@ -47,8 +47,14 @@
 //         operand and the (<= 16) tokens as the B operand (the
 //         "T.gemm(A_s, B_h, acc, transpose_B=True)" of the TileLang loop), in
 //         bf16 for bf16 weights and in f16 for FP8 weights.
-// Two accumulator sets alternate over the K steps (shorter dependency chains);
-// they are added in a fixed order.
+//   TC:   (FP8, opt-in) 5th-generation tensor cores: an MMA warp issues
+//         tcgen05.mma kind::f8f6f4 with the e4m3 weight tile, as TMA wrote it,
+//         as the A operand and an exact three-part e4m3 split of x as B; the
+//         fp32 accumulators live in tensor memory and warps 0-3 read them back.
+//         Correct and tested, but slower here than MMA (a stage is released
+//         only once the tensor core has read it).
+// SIMT and MMA keep two accumulator sets alternating over the K steps
+// (shorter dependency chains), added in a fixed order.
 //
 // Split-K fix-up.  Within one segment the units of one tile form a "run".  A
 // run that covers its whole tile is finished on the spot: every warp rounds
@@ -78,6 +84,12 @@
 //
 // Every wait is bounded (mbarrier waits give up after ~2 s, set a bit of the
 // device error word and make the CTA leave in an orderly way).
+//
+// Next-layer activation copy.  Inside one decode stream, a plain linear whose
+// y is exactly the x of a following FP8 layer also writes that layer's exact
+// f16 copy (xh_next): every output tile is one 128-column K block of it, made
+// by the fix-up (one warp per token) next to y; tiles one segment covers whole
+// go through per-CTA slots and a bounded meeting of the consumer warps.
 #pragma once
 
 #include "dl_device.cuh"
