@@ -125,7 +125,10 @@ struct Plan {
 };
 
 int auto_family(int dtype, int M) {
-    if (dtype == DL_BF16) return M <= 2 ? dl::kSIMT : dl::kMMA;
+    // bf16: CUDA-core FMAs at one token, the MMA family from two (same-box
+    // bench: gate_up + down at M = 2 run at 0.989 of the copy peak with the
+    // MMA family against 0.969 with the CUDA-core one; equal at M = 1).
+    if (dtype == DL_BF16) return M <= 1 ? dl::kSIMT : dl::kMMA;
     return dl::kMMA;
 }
 
