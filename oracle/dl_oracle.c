@@ -10,9 +10,9 @@
  *
  * in IEEE double, with k ascending.  This is the linear layer y = x W^T of
  * "Multi-GPU Inference and Serving at Scale" (Example 2, a column split: a
- * linear layer computes y = x W) with W stored [N, K] ("transpose_B" in the
- * TileLang loop of "9% faster GLM-5.3-Flash prefill with GPU-to-GPU IPC",
- * section "TileLang: twice as fast, and no faster").  A k sub-range gives the
+ * linear layer computes y = x W) with W stored [N, K], the weight rows taken
+ * as columns as in the TileLang loop of "9% faster GLM-5.3-Flash prefill with
+ * GPU-to-GPU IPC", section "TileLang: twice as fast, and no faster").  A k sub-range gives the
  * partial sum one device holds under a row split (same page, Example 3).
  *
  *   X(m,k)  = the bf16 activation, decoded exactly (its 16 bits are the top

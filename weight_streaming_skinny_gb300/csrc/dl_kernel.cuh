@@ -10,8 +10,8 @@
 // of about one CTA per SM takes segment blockIdx.x of the first wave and then
 // claims further segments, in order, from an atomic counter, so SMs that
 // happen to stream faster take more of the small segments and all of them
-// finish together.  This is the "split the long dimension across blocks so
-// the whole chip streams weights" of "9% faster GLM-5.3-Flash prefill with
+// finish together.  It spreads the long dimension over blocks so that every
+// SM streams weights, as in "9% faster GLM-5.3-Flash prefill with
 // GPU-to-GPU IPC" (section "TileLang: twice as fast, and no faster", where a
 // 1..6-token step otherwise launches 16-96 blocks for 188 SMs), balanced at
 // run time.
@@ -22,7 +22,7 @@
 // unit's block scale and the per-token unscale factors of its activations,
 // copied asynchronously on the same barrier).  The weight tile is copied as
 // 128 rows x 128 bytes with the 128-byte swizzle.  Warps 0-7 each own 16
-// weight rows of the tile (the TileLang loop's T.Pipelined(..., num_stages=2),
+// weight rows of the tile (the TileLang loop's two-stage software pipeline,
 // deepened to cover GB300's HBM latency).  Every weight byte is read from HBM
 // exactly once per call.
 //
@@ -45,7 +45,8 @@
 //         halves at the end of a run.
 //   MMA:  warp-level mma.sync m16n8k16 -> fp32 with the weights as the 16-row A
 //         operand and the (<= 16) tokens as the B operand (the
-//         "T.gemm(A_s, B_h, acc, transpose_B=True)" of the TileLang loop), in
+//         16-bit GEMM of the TileLang loop, activations against the
+//         dequantised weight tile with the weights' rows as columns), in
 //         bf16 for bf16 weights and in f16 for FP8 weights.
 //   TC:   (FP8, opt-in) 5th-generation tensor cores: an MMA warp issues
 //         tcgen05.mma kind::f8f6f4 with the e4m3 weight tile, as TMA wrote it,
@@ -69,8 +70,8 @@
 // ascending K), add the bias, round once and reset the ticket.  No CTA ever waits for another, and the order of every sum is fixed
 // by the partition alone, so results are bitwise reproducible whichever CTA
 // computed which segment.  Inside one GPU this plays the role of the
-// row-parallel "partial sums, then all-reduce" of "Multi-GPU Inference and
-// Serving at Scale", Example 3.
+// row-parallel split of "Multi-GPU Inference and Serving at Scale", Example 3,
+// whose partial sums an all-reduce adds.
 //
 // Dependent launch.  The kernel lets the next kernel on the stream launch as
 // soon as it starts (griddepcontrol.launch_dependents); all its threads but
