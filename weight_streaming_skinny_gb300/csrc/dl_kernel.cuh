@@ -4,17 +4,18 @@
 // each tile's K range is cut into units of 32 KB of weights: 128 columns of
 // bf16, or 256 columns (two 128x128 scale blocks) of FP8.  The U = tiles x
 // units-per-tile units, in tile-major order, are cut into
-// contiguous segments by a partition fixed by (M, N, K, SM count) alone: a
-// first wave of one large segment per CTA (about 7/8 of the work), then waves
-// of segments that halve in size down to a small minimum.  A persistent grid
-// of about one CTA per SM takes segment blockIdx.x of the first wave and then
-// claims further segments, in order, from an atomic counter, so SMs that
-// happen to stream faster take more of the small segments and all of them
-// finish together.  It spreads the long dimension over blocks so that every
-// SM streams weights, as in "9% faster GLM-5.3-Flash prefill with
-// GPU-to-GPU IPC" (section "TileLang: twice as fast, and no faster", where a
-// 1..6-token step otherwise launches 16-96 blocks for 188 SMs), balanced at
-// run time.
+// contiguous segments by a partition fixed by (dtype, M, N, K, SM count)
+// alone.  A persistent grid of about one CTA per SM takes segment blockIdx.x
+// of the first wave.  For FP8 that wave is the whole partition: a static
+// balanced split, every CTA within one unit of the others.  For bf16 the first
+// wave holds about 7/8 of the work and waves of segments that halve in size
+// down to a small minimum follow; CTAs claim those in order from an atomic
+// counter, so SMs that happen to stream faster take more of the small
+// segments and all of them finish together.  Either way the long dimension is
+// spread over blocks so that every SM streams weights, as in "9% faster
+// GLM-5.3-Flash prefill with GPU-to-GPU IPC" (section "TileLang: twice as
+// fast, and no faster", where a 1..6-token step otherwise launches 16-96
+// blocks for 188 SMs).
 //
 // Pipeline.  Warp 8 (one elected thread) streams units HBM -> shared memory
 // with TMA tensor copies into a ring of `stages` buffers guarded by full/empty
@@ -1404,6 +1405,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     if (++ls == S) { ls = 0; lph ^= 1u; }
                 }
                 if (!ok) break;
+                if (p.n_segments == G) break;      // static partition: nothing to claim
                 // Claim only when at most kClaimDepth issued stages are still
                 // unconsumed, so that no CTA holds a long backlog when the
                 // shared segments run out: wait for stage issued - kClaimDepth
