@@ -17,9 +17,10 @@
  * dimension split across blocks so that the whole chip streams weights).
  *
  * w(n, k) is either the bf16 weight W[n][k], or, for weight-only FP8,
- * e4m3(Wq[n][k]) * scales[n / 128][k / 128]: the OCP E4M3FN code decoded
- * exactly and multiplied by the fp32 scale of its 128x128 block (the TileLang
- * loop's "B_h[i,k] = B_s[i,k] * S[nb, (kb*BK + k) // 128]").  Activations are
+ * e4m3(Wq[n][k]) * scales[n / 128][k / 128]: each e4m3 weight (OCP E4M3FN,
+ * decoded exactly) times the fp32 scale of the 128x128 block it lies in, the
+ * dequantisation of the same TileLang section, where the weight tile is
+ * multiplied by its block's scale before the 16-bit GEMM.  Activations are
  * never quantised (weight-only FP8; same engine page, §6.2).
  *
  * Conventions for every entry point below:
@@ -60,7 +61,7 @@
 extern "C" {
 #endif
 
-#define DL_VERSION 2
+#define DL_VERSION 3
 
 /* Leading workspace bytes that must be zero before a call (see conventions). */
 #define DL_WORKSPACE_ZERO_BYTES (256u + 16384u * 4u)
@@ -158,9 +159,18 @@ dl_status dl_linear_fp8_block128(const void* x, const void* Wq, const float* sca
  *   DL_STATIC_SCRATCH_BYTES of scratch (dl_workspace_bytes(M, N, K, DL_BF16)
  *   tells) are rejected with DL_ERR_WORKSPACE before anything is enqueued.  The
  *   limit covers every Qwen2.5-72B decoder linear and the lm_head at M <= 8.
- * Set-up: the first call on each device, with that device current, looks up
- *   the array's device address (cudaGetSymbolAddress); make that first call
- *   before any stream capture begins.
+ * Set-up and cost: the array is part of the library's device code, so every
+ *   process that loads the library reserves DL_STATIC_SCRATCH_BYTES on each
+ *   device where that code is loaded -- whether or not it ever calls this
+ *   entry point -- until the process exits.  With CUDA's lazy module loading
+ *   (the default) the code, and so the array, may be placed on a device only
+ *   by the first call that needs it, possibly this entry point's first call.
+ *   That first call on each device, with that device current, also looks up
+ *   the array's device address (cudaGetSymbolAddress) and caches it per device
+ *   index.  Make that first call outside latency-critical code and before any
+ *   stream capture begins.  The cached address does not survive a context
+ *   reset (cudaDeviceReset): do not call this entry point on a device after
+ *   resetting it in the same process.
  * Sharing: every call on a device uses the same array, which keeps what the
  *   last call left.  Each call first clears (cudaMemsetAsync on `stream`) the
  *   arrival counters that must start at zero; the partial sums need no
@@ -271,8 +281,15 @@ size_t dl_decode_stream_workspace_bytes(const dl_layer* layers, int n_layers);
  */
 int dl_decode_stream_launches(const dl_layer* layers, int n_layers, size_t ws_bytes);
 
-/* Destroy every cached graph (host call; synchronises nothing). */
+/*
+ * Destroy every cached graph (host call; synchronises nothing: a graph still
+ * running is freed once its launches complete).  The cache keeps at most 16
+ * graphs and drops the least recently used one when a new list is captured.
+ */
 void dl_graph_cache_clear(void);
+
+/* Number of graphs currently cached by dl_decode_stream (host call). */
+int dl_graph_cache_size(void);
 
 /*
  * Process-wide tuning overrides, for tests and tuning; 0 = automatic.
@@ -283,17 +300,39 @@ void dl_graph_cache_clear(void);
  *   max_ctas     upper bound on the grid (1 = a single CTA)
  * Changing an override changes dl_workspace_bytes and may change the last
  * bits of results (a different split of K); any setting is correct.
+ * ctas_per_sm = 2 is not applied to FP8 calls with more than 8 tokens (16
+ * staged token rows): they keep one CTA per SM.
  * Not thread-safe against concurrent launches.
  */
 dl_status dl_set_override(int kernel, int ctas_per_sm, int max_ctas);
+
+/*
+ * Test hooks for the bounded device waits, applied to later launches
+ * (process-wide, like the overrides; 0, 0 restores normal operation):
+ *   wait_limit_ns   how long every device-side wait waits before it gives up,
+ *                   sets its bit of the device error word and lets its CTA
+ *                   leave (0 = the default, about 2 s);
+ *   withhold_stage  k >= 1: CTA 0 of every later linear-layer launch opens its
+ *                   k-th pipeline stage (the stage's barrier expects its
+ *                   bytes) but never issues the copies that would fill it, so
+ *                   every wait on that stage runs out; no copy is in flight
+ *                   for it when the CTA leaves.  Needs 0 < wait_limit_ns <=
+ *                   100 ms (else DL_ERR_INVALID_ARG).
+ * A launch that ran with a withheld stage leaves wrong outputs and may leave
+ * arrival counters set in its workspace: zero the workspace's first
+ * DL_WORKSPACE_ZERO_BYTES before using it again, and read the error word with
+ * dl_device_status.  Not thread-safe against concurrent launches.
+ */
+dl_status dl_set_wait_test(long long wait_limit_ns, int withhold_stage);
 
 /*
  * Read and clear the device error word of the current device: bit 0 = a
  * consumer gave up waiting for a weight tile, bit 1 = the loader gave up
  * waiting for a free stage, bit 2 = the final wait for copies in flight gave
  * up, bit 3 = a hand-over of a split-K run between the consumer warps and the
- * ticket warp gave up.  Every device wait is bounded (about 2 s); a kernel that gives up sets a
- * bit and returns instead of hanging.  SYNCHRONISES the device.  *flags may
+ * ticket warp gave up.  Every device wait is bounded (about 2 s, or the limit
+ * set with dl_set_wait_test); a kernel that gives up sets a bit and returns
+ * instead of hanging.  SYNCHRONISES the device.  *flags may
  * be NULL.  Returns DL_ERR_DEVICE if any bit was set.
  */
 dl_status dl_device_status(unsigned int* flags);

@@ -10,7 +10,8 @@ import weight_streaming_skinny_gb300 as dl
 EXPECTED = {"dl_workspace_bytes", "dl_linear_bf16", "dl_linear_fp8_block128", "dl_decode_stream",
             "dl_graph_cache_clear", "dl_set_override", "dl_device_status", "dl_last_error",
             "dl_version", "dl_linear_swiglu", "dl_linear_bf16_static_scratch", "dl_linear_argmax",
-            "dl_decode_stream_workspace_bytes", "dl_decode_stream_launches"}
+            "dl_decode_stream_workspace_bytes", "dl_decode_stream_launches", "dl_set_wait_test",
+            "dl_graph_cache_size"}
 
 
 def test_library_exports_every_header_symbol():
@@ -156,3 +157,20 @@ def test_argmax_validation_before_any_cuda_call():
                                 None, 1, 256, 128, ws, 1 << 20, None) == 3
     assert lib.dl_linear_argmax(0, p, p, None, None, p, None, None, None, 17, 256, 128, ws,
                                 1 << 20, None) == 2
+
+
+def test_wait_test_hook_validation():
+    """The bounded-wait test hooks: a withheld stage needs a short wait limit."""
+    lib = dl.load()
+    assert lib.dl_set_wait_test(-1, 0) == 1
+    assert lib.dl_set_wait_test(0, -1) == 1
+    assert lib.dl_set_wait_test(0, 2) == 1               # withholding needs a limit ...
+    assert lib.dl_set_wait_test(10**9, 2) == 1           # ... of at most 100 ms
+    assert b"100 ms" in lib.dl_last_error()
+    assert lib.dl_set_wait_test(20_000_000, 2) == 0
+    assert lib.dl_set_wait_test(0, 0) == 0
+
+
+def test_graph_cache_empty_without_a_gpu_call():
+    dl.graph_cache_clear()
+    assert dl.graph_cache_size() == 0

@@ -23,7 +23,7 @@ __all__ = [
     "linear_swiglu", "linear_argmax", "interleave_gate_up", "ABI_VERSION",
     "linear_bf16_static_scratch", "STATIC_SCRATCH_BYTES", "WORKSPACE_ZERO_BYTES",
     "linear_fp8_block128", "decode_stream", "decode_stream_workspace_bytes",
-    "decode_stream_launches", "graph_cache_clear",
+    "decode_stream_launches", "graph_cache_clear", "graph_cache_size", "set_wait_test",
     "set_override",
     "device_status", "exported_symbols", "header_symbols",
 ]
@@ -56,7 +56,7 @@ class _Layer(ctypes.Structure):
                 ("scales", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("act", ctypes.c_int)]
 
-ABI_VERSION = 2   # DL_VERSION this binding marshals for
+ABI_VERSION = 3   # DL_VERSION this binding marshals for
 
 
 def library_path() -> str:
@@ -85,6 +85,9 @@ def load():
         lib.dl_decode_stream.argtypes = [ctypes.POINTER(_Layer), i, vp, sz, vp, i]
         lib.dl_decode_stream.restype = i
         lib.dl_graph_cache_clear.restype = None
+        lib.dl_graph_cache_size.restype = i
+        lib.dl_set_wait_test.argtypes = [ctypes.c_longlong, i]
+        lib.dl_set_wait_test.restype = i
         lib.dl_decode_stream_workspace_bytes.argtypes = [ctypes.POINTER(_Layer), i]
         lib.dl_decode_stream_workspace_bytes.restype = sz
         lib.dl_decode_stream_launches.argtypes = [ctypes.POINTER(_Layer), i, sz]
@@ -454,6 +457,17 @@ def decode_stream_launches(layers, workspace: Workspace) -> int:
 
 def graph_cache_clear():
     load().dl_graph_cache_clear()
+
+
+def graph_cache_size() -> int:
+    """Graphs currently cached by decode_stream(use_graph=True)."""
+    return int(load().dl_graph_cache_size())
+
+
+def set_wait_test(wait_limit_ns: int = 0, withhold_stage: int = 0):
+    """Test hooks of the bounded device waits (see dl_set_wait_test): the wait
+    limit of later launches and a stage CTA 0 withholds; (0, 0) turns them off."""
+    _check(load().dl_set_wait_test(int(wait_limit_ns), int(withhold_stage)))
 
 
 def set_override(kernel: int = 0, ctas_per_sm: int = 0, max_ctas: int = 0):

@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <list>
 #include <map>
 #include <mutex>
 #include <string>
@@ -47,6 +48,10 @@ dl_status ok() {
 std::atomic<int> g_kernel_override{0};
 std::atomic<int> g_cps_override{0};
 std::atomic<int> g_max_ctas_override{0};
+// Test hooks of the bounded device waits (dl_set_wait_test): the limit of
+// every wait (0: the default) and the stage CTA 0 withholds (0: none).
+std::atomic<long long> g_wait_ns_override{0};
+std::atomic<int> g_withhold_override{0};
 
 constexpr int kMaxStages = 16;
 // bf16 work partition (see make_plan): share of the units in the first wave,
@@ -179,7 +184,12 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     const int dt_k = dtype == DL_BF16 ? dl::kBF16 : dl::kFP8;
     const int fits = dl::host_min_blocks(dt_k, pl.family, pl.mt);
     const int cps_o = g_cps_override.load();
-    const int cps = cps_o ? cps_o : fits;
+    int cps = cps_o ? cps_o : fits;
+    // Two CTAs per SM stay away from FP8 weights at 16 staged tokens: the one
+    // GPU fault ever recorded for this library came from that combination
+    // (a build compiled for two resident CTAs, first FP8 16-token call), and
+    // reading the code has not explained it.  Such calls keep one CTA per SM.
+    if (cps == 2 && dtype == DL_FP8_B128 && pl.mt == 16) cps = 1;
     const bool half_smem = cps == 2;
     long long grid = (long long)di.sm_count * cps;
     const int mc = g_max_ctas_override.load();
@@ -476,6 +486,9 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
     p.wave_seg0[dl::kMaxWaves] = pl.wave_seg0[pl.n_waves];
     p.stages = pl.stages;
     p.err = di.err_word;
+    const long long wait_o = g_wait_ns_override.load();
+    p.wait_ns = wait_o > 0 ? (unsigned long long)wait_o : dl::kWaitLimitNs;
+    p.withhold = g_withhold_override.load();
     p.xh_next = xh_next;
     p.us_next = us_next;
     p.wslot = wslot;
@@ -656,8 +669,30 @@ dl_status plan_stream(const dl_layer* layers, int n, const DeviceInfo& di, size_
 
 // ----------------------------------------------------------------- graph cache
 
+// Cached executable graphs of dl_decode_stream, least recently used first
+// out.  The key is built from the layers' fields (never from the struct's
+// raw bytes, whose padding a C caller may leave uninitialised).
+constexpr size_t kGraphCacheSize = 16;
 std::mutex g_graph_mu;
-std::map<std::string, cudaGraphExec_t> g_graphs;
+std::list<std::pair<std::string, cudaGraphExec_t>> g_graph_lru;   // most recent first
+std::map<std::string, std::list<std::pair<std::string, cudaGraphExec_t>>::iterator> g_graphs;
+
+std::string graph_key(const dl_layer* layers, int n, const void* ws, size_t ws_bytes, int dev) {
+    std::vector<long long> k;
+    k.reserve((size_t)n * 10 + 10);
+    for (int i = 0; i < n; ++i) {
+        const dl_layer& L = layers[i];
+        k.insert(k.end(), {(long long)L.dtype, (long long)L.M, (long long)L.N, (long long)L.K,
+                           (long long)L.act, (long long)(uintptr_t)L.x, (long long)(uintptr_t)L.W,
+                           (long long)(uintptr_t)L.scales, (long long)(uintptr_t)L.bias,
+                           (long long)(uintptr_t)L.y});
+    }
+    k.insert(k.end(), {(long long)(uintptr_t)ws, (long long)ws_bytes, (long long)dev,
+                       (long long)g_kernel_override.load(), (long long)g_cps_override.load(),
+                       (long long)g_max_ctas_override.load(), g_wait_ns_override.load(),
+                       (long long)g_withhold_override.load()});
+    return std::string(reinterpret_cast<const char*>(k.data()), k.size() * sizeof(long long));
+}
 
 }  // namespace
 
@@ -899,16 +934,15 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
         return fail(DL_ERR_INVALID_ARG, "graph replay needs a non-default stream");
     int dev = 0;
     cudaGetDevice(&dev);
-    std::string key(reinterpret_cast<const char*>(layers), sizeof(dl_layer) * (size_t)n_layers);
-    const long long extra[6] = {(long long)(uintptr_t)workspace, (long long)ws_bytes, dev,
-                                g_kernel_override.load(), g_cps_override.load(),
-                                g_max_ctas_override.load()};
-    key.append(reinterpret_cast<const char*>(extra), sizeof extra);
+    const std::string key = graph_key(layers, n_layers, workspace, ws_bytes, dev);
     cudaGraphExec_t exec = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_graph_mu);
         auto it = g_graphs.find(key);
-        if (it != g_graphs.end()) exec = it->second;
+        if (it != g_graphs.end()) {
+            g_graph_lru.splice(g_graph_lru.begin(), g_graph_lru, it->second);   // now most recent
+            exec = it->second->second;
+        }
     }
     cudaError_t e;
     if (!exec) {
@@ -926,7 +960,21 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return fail(DL_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
         std::lock_guard<std::mutex> lk(g_graph_mu);
-        g_graphs[key] = exec;
+        auto it = g_graphs.find(key);
+        if (it != g_graphs.end()) {            // another thread cached the same list meanwhile
+            cudaGraphExecDestroy(it->second->second);
+            it->second->second = exec;
+            g_graph_lru.splice(g_graph_lru.begin(), g_graph_lru, it->second);
+        } else {
+            if (g_graph_lru.size() >= kGraphCacheSize) {
+                // A graph still in flight is freed once its launches complete.
+                cudaGraphExecDestroy(g_graph_lru.back().second);
+                g_graphs.erase(g_graph_lru.back().first);
+                g_graph_lru.pop_back();
+            }
+            g_graph_lru.emplace_front(key, exec);
+            g_graphs[key] = g_graph_lru.begin();
+        }
     }
     if ((e = cudaGraphLaunch(exec, st)) != cudaSuccess)
         return fail(DL_ERR_CUDA, "cudaGraphLaunch: %s", cudaGetErrorString(e));
@@ -971,8 +1019,25 @@ int dl_decode_stream_launches(const dl_layer* layers, int n_layers, size_t ws_by
 
 void dl_graph_cache_clear(void) {
     std::lock_guard<std::mutex> lk(g_graph_mu);
-    for (auto& kv : g_graphs) cudaGraphExecDestroy(kv.second);
+    for (auto& kv : g_graph_lru) cudaGraphExecDestroy(kv.second);
+    g_graph_lru.clear();
     g_graphs.clear();
+}
+
+int dl_graph_cache_size(void) {
+    std::lock_guard<std::mutex> lk(g_graph_mu);
+    return (int)g_graph_lru.size();
+}
+
+dl_status dl_set_wait_test(long long wait_limit_ns, int withhold_stage) {
+    if (wait_limit_ns < 0) return fail(DL_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
+    if (withhold_stage < 0) return fail(DL_ERR_INVALID_ARG, "withhold_stage must be >= 0");
+    if (withhold_stage > 0 && (wait_limit_ns <= 0 || wait_limit_ns > 100000000LL))
+        return fail(DL_ERR_INVALID_ARG,
+                    "withholding a stage needs a wait limit in (0, 100 ms] (got %lld ns)", wait_limit_ns);
+    g_wait_ns_override.store(wait_limit_ns);
+    g_withhold_override.store(withhold_stage);
+    return ok();
 }
 
 dl_status dl_device_status(unsigned int* flags) {

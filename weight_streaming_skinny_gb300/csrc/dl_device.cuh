@@ -15,8 +15,16 @@ constexpr unsigned kErrProducerWait = 2u;
 constexpr unsigned kErrDrainWait = 4u;
 constexpr unsigned kErrRunWait = 8u;     // split-run hand-over (ticket warp / consumers)
 
-// Every device-side wait gives up after this long and reports an error bit.
+// Every device-side wait gives up after this long (unless a launch asks for
+// another limit) and reports an error bit.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Where a bounded wait reports that it gave up (the device error word) and
+// how long it waits first.
+struct WaitCtl {
+    unsigned* word;
+    unsigned long long limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -63,9 +71,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, ORs `err_bit` into the device error word and returns false.
+// w.limit_ns, ORs `err_bit` into the device error word and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  unsigned* err_word, unsigned err_bit) {
+                                                  const WaitCtl& w, unsigned err_bit) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
         if (mbar_try_wait(bar, parity)) return true;
@@ -73,8 +81,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 #pragma unroll 1
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(err_word, err_bit);
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            atomicOr(w.word, err_bit);
             return false;
         }
     }

@@ -164,6 +164,9 @@ struct LinearParams {
     int early_stages;         // stages whose weights may be fetched before griddepcontrol.wait
                               //   (0: the previous kernel may write weights)
     unsigned* err;            // device error word (bounded waits OR their bit in)
+    unsigned long long wait_ns;   // how long a device wait waits before it gives up
+    int withhold;             // test hook: k >= 1 = CTA 0 opens its k-th stage but never
+                              //   issues the copies that fill it (0: off)
     // The exact f16 copy of y for a next FP8 layer whose x is this layer's y
     // (act 0, N % 128 == 0; its copy has the same staged token rows MTB):
     // xh_next [N/128][2][MTB][64] and us_next [N/128][16], written by the
@@ -1169,7 +1172,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const int KB = p.KB;
     const int UT = p.UT;
     constexpr int kUnitKB = DT == kBF16 ? 1 : kMaxUnitsPerStage;   // K blocks per unit
-    unsigned* err = p.err;
+    const WaitCtl err{p.err, p.wait_ns};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -1357,6 +1360,13 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 mbar_arrive_expect_tx(bar, bytes);
             };
 
+            // Test hook for the bounded waits: CTA 0 opens its p.withhold-th
+            // stage (the barrier expects the bytes) but never issues the
+            // copies that would fill it, so every wait on that stage runs out
+            // with nothing in flight for it.
+            auto withheld = [&](long long idx) -> bool {
+                return p.withhold > 0 && blockIdx.x == 0 && idx + 1 == p.withhold;
+            };
             int seg = blockIdx.x;
             long long u0 = seg_begin(p, seg);
             long long u1 = seg_begin(p, seg + 1);
@@ -1371,13 +1381,13 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 int ptile = tile, pku = ku;
                 for (; pre < S && pre < p.early_stages && pre < left; ++pre) {
                     open_stage(pre, ptile, pku, seg, pre == 0, left - pre);
-                    issue_w(pre, ptile, pku * kUnitKB, blocks_of(pku));
+                    if (!withheld(pre)) issue_w(pre, ptile, pku * kUnitKB, blocks_of(pku));
                     if (++pku == UT) { pku = 0; ++ptile; }
                 }
             }
             griddep_wait();
             for (int st = 0; st < pre; ++st) {
-                issue_x(st, ku * kUnitKB, blocks_of(ku));
+                if (!withheld(st)) issue_x(st, ku * kUnitKB, blocks_of(ku));
                 if (++ku == UT) { ku = 0; ++tile; }
             }
             left -= pre;
@@ -1397,8 +1407,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         break;
                     }
                     open_stage(ls, tile, ku, seg, seg_first, left);
-                    issue_w(ls, tile, ku * kUnitKB, blocks_of(ku));
-                    issue_x(ls, ku * kUnitKB, blocks_of(ku));
+                    if (!withheld(issued)) {
+                        issue_w(ls, tile, ku * kUnitKB, blocks_of(ku));
+                        issue_x(ls, ku * kUnitKB, blocks_of(ku));
+                    }
                     seg_first = false;
                     if (++ku == UT) { ku = 0; ++tile; }
                     ++issued;
