@@ -415,6 +415,18 @@ def test_qwen_layer_fp8_m6_sampled(cuda_device, name):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("name", ["qkv", "o"])
+def test_qwen_layer_fp8_m1_sampled(cuda_device, name):
+    """FP8 QKV (with bias) and O at M=1, the shapes of the whole-model stream
+    (gate_up and down at M=1 are in the token sweep)."""
+    L = _full_layer(inputs.DTYPE_FP8_B128, name, 1, 4, cuda_device)
+    y, y32 = run_gpu(L, cuda_device)
+    rows = sample_rows(L.N, seed=4)
+    ref, a = oracle_for(L, rows=rows)
+    assert_parity(y, y32, ref, a, rows=rows, what=f"fp8 M=1 {name}")
+
+
+@pytest.mark.slow
 @pytest.mark.parametrize("dtype", [inputs.DTYPE_BF16, inputs.DTYPE_FP8_B128])
 @pytest.mark.parametrize("name", ["gate_up", "down"])
 def test_token_sweep_sampled(cuda_device, dtype, name):
