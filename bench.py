@@ -152,7 +152,10 @@ class ClockSampler:
 MLP_TOKENS = (1, 2, 4, 6, 8, 16)
 # The token sweep: the two largest linears of a decoder layer (gate_up, down)
 # at M = 1..16 tokens, each dtype.
-WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8_m1"] + [
+# qwen72b_decoder_fp8_m1 / qwen72b_lm_head_bf16_m1: one decoder layer and the
+# lm_head of the whole-model stream on their own (small cases of its launches).
+WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8_m1",
+             "qwen72b_decoder_fp8_m1", "qwen72b_lm_head_bf16_m1"] + [
     f"qwen72b_mlp_{dt}_m{m}" for dt in ("bf16", "fp8") for m in MLP_TOKENS]
 
 
@@ -166,15 +169,19 @@ def layer_specs(workload: str):
         return [(inputs.DTYPE_BF16, 1, *shapes[n][:2], shapes[n][2], n, 0) for n in shapes], 1
     if workload == "qwen72b_layer_fp8_m6":
         return [(inputs.DTYPE_FP8_B128, 6, *shapes[n][:2], shapes[n][2], n, 0) for n in shapes], 2
-    if workload == "qwen72b_model_fp8_m1":
+    if workload in ("qwen72b_model_fp8_m1", "qwen72b_decoder_fp8_m1"):
         specs = []
-        for layer in range(inputs.QWEN72B_LAYERS):
+        for layer in range(inputs.QWEN72B_LAYERS if workload == "qwen72b_model_fp8_m1" else 1):
             for n in shapes:
                 specs.append((inputs.DTYPE_FP8_B128, 1, *shapes[n][:2], shapes[n][2], f"{n}.{layer}",
                               1 if n == "gate_up" else 0))
-        N, K, b = inputs.QWEN72B_LM_HEAD
-        specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 2))
+        if workload == "qwen72b_model_fp8_m1":
+            N, K, b = inputs.QWEN72B_LM_HEAD
+            specs.append((inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 2))
         return specs, 4
+    if workload == "qwen72b_lm_head_bf16_m1":
+        N, K, b = inputs.QWEN72B_LM_HEAD
+        return [(inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 2)], 4
     if workload.startswith("qwen72b_mlp_"):
         _, _, dt, m = workload.split("_")
         dtype = inputs.DTYPE_BF16 if dt == "bf16" else inputs.DTYPE_FP8_B128
@@ -215,7 +222,7 @@ def build_layers(workload, dev):
         L = inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg, layer_idx=i, device=dev)
         L.act = act
         out.append((name, L))
-    if workload == "qwen72b_model_fp8_m1":
+    if workload in ("qwen72b_model_fp8_m1", "qwen72b_decoder_fp8_m1"):
         for i in range(1, len(out)):
             prev, cur = out[i - 1][1], out[i][1]
             if out_cols(prev) == cur.K and prev.M == cur.M and out[i][0].split(".")[0] != "o":
@@ -290,12 +297,16 @@ def time_steps(torch, step, stream, steps, per_step=True):
 def single_call_times(torch, dl, calls, stream, reps):
     """Isolated call times: an event pair around every call (events break the
     overlap with the neighbouring launches), calls cycled through `calls`
-    (distinct weights keep L2 cold).  Returns per-call ms."""
+    (distinct weights keep L2 cold).  A short spin kernel before each pair
+    keeps the GPU busy while the host enqueues the call, so that the pair
+    measures the call on the device, not the host's submission.  Returns
+    per-call ms."""
     n = len(calls)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
     with torch.cuda.stream(stream):
         for r in range(reps):
+            torch.cuda._sleep(100_000)
             evs[r][0].record(stream)
             calls[r % n]()
             evs[r][1].record(stream)
@@ -725,12 +736,13 @@ def main():
         if rank != 0:
             return
         import torch
-        if args.workload == "qwen72b_model_fp8_m1":
-            # bounded sample: decoder layer 0 and the lm_head (not 72 GB of host weights)
+        if args.workload in ("qwen72b_model_fp8_m1", "qwen72b_decoder_fp8_m1"):
+            # bounded sample: decoder layer 0 (and the lm_head), each layer
+            # with its own seeded x (not 72 GB of host weights)
             from weight_streaming_skinny_gb300 import inputs
             specs_all, cfg = layer_specs(args.workload)
             layers = []
-            for i in (0, 1, 2, 3, len(specs_all) - 1):
+            for i in sorted({0, 1, 2, 3, len(specs_all) - 1}):
                 dt, M, N, K, bias, name, act = specs_all[i]
                 Lh = inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg, layer_idx=i, device="cpu")
                 Lh.act = act
