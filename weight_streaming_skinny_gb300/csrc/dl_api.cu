@@ -58,6 +58,12 @@ constexpr int kMaxStages = 16;
 // the smallest later segment in units, and whether later segments are aligned
 // to divisors of the units per tile.
 constexpr long long kFirstWaveNum = 7, kFirstWaveDen = 8;
+// bf16 layers with at most this many units per CTA take FP8's static split
+// (same box, two runs each: the bf16 decoder-layer step 0.2691 -> 0.2667 ms,
+// gate_up + down at 16 tokens 0.2226 -> 0.2208 ms, one token unchanged; a
+// limit of 64 gained less, 32 nothing): a few small claimed segments at the
+// end cost such layers more than the balance they buy.
+constexpr long long kStaticSplitMaxUnitsPerCta = 128;
 constexpr long long kMinSegUnits = 8;
 constexpr bool kAlignSegments = true;
 // Layers of a stream whose FP8 activation copies may be made ahead (a bounded
@@ -200,7 +206,8 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     // Segments: a fixed partition of the units, summed by the fix-up in segment
     // order.  CTA b takes segment b (the first wave, one per CTA).
     //
-    // FP8: that is all -- a static balanced split, U mod G CTAs with one unit
+    // FP8, and bf16 layers of at most kStaticSplitMaxUnitsPerCta units per
+    // CTA: that is all -- a static balanced split, U mod G CTAs with one unit
     // more than the others, no segment claimed at run time.  Measured against
     // the bf16 scheme below: FP8 M = 6 layer step 0.1644 -> 0.1544 ms, the
     // 80-layer model 13.13 -> 12.26 ms per token, gate_up + down 0.1298 ->
@@ -222,7 +229,7 @@ dl_status make_plan(int dtype, int M, int N, int K, const DeviceInfo& di, Plan& 
     // multiple of b (an alignment segment of fewer than b units follows the
     // first wave if needed) and holds multiples of b: its segments end on tile
     // boundaries or at multiples of b inside a tile.
-    if (dtype == DL_FP8_B128) {
+    if (dtype == DL_FP8_B128 || pl.units <= (long long)pl.grid * kStaticSplitMaxUnitsPerCta) {
         const long long G = pl.grid, U = pl.units;
         const long long sz = U / G, r = U % G;     // grid <= units, so sz >= 1
         int w = 0;

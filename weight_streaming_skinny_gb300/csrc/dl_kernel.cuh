@@ -6,12 +6,13 @@
 // units-per-tile units, in tile-major order, are cut into
 // contiguous segments by a partition fixed by (dtype, M, N, K, SM count)
 // alone.  A persistent grid of about one CTA per SM takes segment blockIdx.x
-// of the first wave.  For FP8 that wave is the whole partition: a static
-// balanced split, every CTA within one unit of the others.  For bf16 the first
-// wave holds about 7/8 of the work and waves of segments that halve in size
-// down to a small minimum follow; CTAs claim those in order from an atomic
-// counter, so SMs that happen to stream faster take more of the small
-// segments and all of them finish together.  Either way the long dimension is
+// of the first wave.  For FP8, and for bf16 layers of at most 128 units per
+// CTA, that wave is the whole partition: a static balanced split, every CTA
+// within one unit of the others.  For larger bf16 layers the first wave holds
+// about 7/8 of the work and waves of segments that halve in size down to a
+// small minimum follow; CTAs claim those in order from an atomic counter, so
+// SMs that happen to stream faster take more of the small segments and all of
+// them finish together.  Either way the long dimension is
 // spread over blocks so that every SM streams weights, as in "9% faster
 // GLM-5.3-Flash prefill with GPU-to-GPU IPC" (section "TileLang: twice as
 // fast, and no faster", where a 1..6-token step otherwise launches 16-96
