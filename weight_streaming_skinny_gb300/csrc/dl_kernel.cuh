@@ -604,12 +604,50 @@ struct MmaConsumer {
         }
     }
 
+    // Fragments of k-steps s and s + 1: the A codes of both steps and their
+    // B fragments (chunks c0 .. c0 + 3 of box s / 4).
+    __device__ __forceinline__ void fp8_load_pair(uint32_t abase, int aswz, int mat, uint32_t sx, int rr,
+                                                  int s, uint32_t (&q)[4], uint32_t (&b)[2][NT][2]) {
+        ldmatrix_x4(abase + (((s + (mat >> 1)) ^ aswz) << 4), q[0], q[1], q[2], q[3]);
+        const uint32_t xbox = sx + (s >> 2) * (MT * 128);
+        const int c0 = (s & 3) * 2;
+        if constexpr (MT == 8) {
+            uint32_t r[4];
+            ldmatrix_x4(xbox + rr * 128 + (((c0 + mat) ^ rr) << 4), r[0], r[1], r[2], r[3]);
+            b[0][0][0] = r[0]; b[0][0][1] = r[1];
+            b[1][0][0] = r[2]; b[1][0][1] = r[3];
+        } else {
+            const int tok = rr + ((mat >> 1) << 3);
+            uint32_t r[4], u[4];
+            ldmatrix_x4(xbox + tok * 128 + (((c0 + (mat & 1)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
+            ldmatrix_x4(xbox + tok * 128 + (((c0 + 2 + (mat & 1)) ^ (tok & 7)) << 4), u[0], u[1], u[2], u[3]);
+            b[0][0][0] = r[0]; b[0][0][1] = r[1]; b[0][1][0] = r[2]; b[0][1][1] = r[3];
+            b[1][0][0] = u[0]; b[1][0][1] = u[1]; b[1][1][0] = u[2]; b[1][1][1] = u[3];
+        }
+    }
+
+    // Decode and multiply the fragments of one k-step pair.
+    __device__ __forceinline__ void fp8_mma_pair(const uint32_t (&q)[4], const uint32_t (&b)[2][NT][2],
+                                                 float (&part)[2][NT][4]) {
+#pragma unroll
+        for (int ss = 0; ss < 2; ++ss) {
+            uint32_t A0, A1, A2, A3;
+            e4m3x4_to_f16x2x2(q[2 * ss], A0, A2);       // row g
+            e4m3x4_to_f16x2x2(q[2 * ss + 1], A1, A3);   // row g + 8
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(part[ss][nt], A0, A1, A2, A3, b[ss][nt][0], b[ss][nt][1]);
+        }
+    }
+
     // One FP8 unit (this warp's 16 rows x 128 codes) as an f16 MMA against the
     // exact f16 copy of x.  Step s is the 16-code chunk s of each row.  Thread
     // (g, t) receives codes 4t..4t+3 of its rows' chunk; they stand for
     // fragment columns {2t, 2t+1} and {2t+8, 2t+9}, and the prep kernel stored
     // x in that order, so the B fragments come from ldmatrix exactly as for
-    // bf16 weights (bank-conflict free on the swizzled tile).
+    // bf16 weights (bank-conflict free on the swizzled tile).  The fragments of
+    // the next k-step pair are loaded before the current pair's MMAs (two
+    // register sets), so that their shared-memory latency overlaps the MMAs.
     __device__ __forceinline__ void fp8_unit_f16(uint32_t abase, int aswz, int mat, uint32_t sx,
                                                  int lane, float (&part)[2][NT][4]) {
         const int rr = lane & 7;
@@ -619,36 +657,14 @@ struct MmaConsumer {
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) part[k][nt][i] = 0.f;
+        uint32_t qa[4], qb[4], ba[2][NT][2], bb[2][NT][2];
+        fp8_load_pair(abase, aswz, mat, sx, rr, 0, qa, ba);
 #pragma unroll
-        for (int s = 0; s < 8; s += 2) {
-            uint32_t q[4];
-            ldmatrix_x4(abase + (((s + (mat >> 1)) ^ aswz) << 4), q[0], q[1], q[2], q[3]);
-            // B fragments of steps s and s + 1: chunks c0 .. c0 + 3 of box s / 4
-            const uint32_t xbox = sx + (s >> 2) * (MT * 128);
-            const int c0 = (s & 3) * 2;
-            uint32_t b[2][NT][2];
-            if constexpr (MT == 8) {
-                uint32_t r[4];
-                ldmatrix_x4(xbox + rr * 128 + (((c0 + mat) ^ rr) << 4), r[0], r[1], r[2], r[3]);
-                b[0][0][0] = r[0]; b[0][0][1] = r[1];
-                b[1][0][0] = r[2]; b[1][0][1] = r[3];
-            } else {
-                const int tok = rr + ((mat >> 1) << 3);
-                uint32_t r[4], u[4];
-                ldmatrix_x4(xbox + tok * 128 + (((c0 + (mat & 1)) ^ (tok & 7)) << 4), r[0], r[1], r[2], r[3]);
-                ldmatrix_x4(xbox + tok * 128 + (((c0 + 2 + (mat & 1)) ^ (tok & 7)) << 4), u[0], u[1], u[2], u[3]);
-                b[0][0][0] = r[0]; b[0][0][1] = r[1]; b[0][1][0] = r[2]; b[0][1][1] = r[3];
-                b[1][0][0] = u[0]; b[1][0][1] = u[1]; b[1][1][0] = u[2]; b[1][1][1] = u[3];
-            }
-#pragma unroll
-            for (int ss = 0; ss < 2; ++ss) {
-                uint32_t A0, A1, A2, A3;
-                e4m3x4_to_f16x2x2(q[2 * ss], A0, A2);       // row g
-                e4m3x4_to_f16x2x2(q[2 * ss + 1], A1, A3);   // row g + 8
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma_f16_16816(part[ss][nt], A0, A1, A2, A3, b[ss][nt][0], b[ss][nt][1]);
-            }
+        for (int s = 0; s < 8; s += 4) {
+            fp8_load_pair(abase, aswz, mat, sx, rr, s + 2, qb, bb);
+            fp8_mma_pair(qa, ba, part);
+            if (s + 4 < 8) fp8_load_pair(abase, aswz, mat, sx, rr, s + 4, qa, ba);
+            fp8_mma_pair(qb, bb, part);
         }
     }
 
