@@ -258,11 +258,12 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
 /*
  * Workspace bytes with which dl_decode_stream makes every FP8 layer's exact
  * f16 activation copy without a prep launch of its own where it can:
- *  - made ahead: an FP8 layer among the first 16 whose x no earlier layer of
- *    the list writes (no byte of its x lies in an earlier layer's y): layer
- *    0's copy just before it, the others in a launch that runs alongside
- *    layer 0 (or, if layer 0 is not such a layer, before it); one region per
- *    such layer;
+ *  - made ahead: an FP8 layer whose x no earlier layer of the list writes (no
+ *    byte of its x lies in an earlier layer's y): layer 0's copy just before
+ *    it, the others in batches, one launch right after every 16th layer
+ *    (layer 16k) holding the copies of layers 16k+1 .. 16k+16 and running
+ *    alongside layer 16k (the first batch before layer 0 if layer 0 is not
+ *    such a layer); one region per such layer;
  *  - made by the layer before: an FP8 layer whose x is exactly the whole y of
  *    the layer just before it, a plain linear (act 0) with the same M (and so
  *    N % 128 == 0): that layer's epilogue writes the copy next to y; two

@@ -2,9 +2,10 @@
 
 An FP8 layer whose x no earlier layer of the list writes has its f16 copy
 made ahead (when the workspace has room, dl_decode_stream_workspace_bytes):
-layer 0's just before it, every later one's in a launch right after layer 0's
-kernel that copies while layer 0 runs.  A layer fed by an earlier layer keeps
-its own prep kernel.  Either way the outputs must equal the single calls' bit
+layer 0's just before it, the later ones' in batches, one launch right after
+every 16th layer (layer 16k) holding the copies of layers 16k+1 .. 16k+16 and
+copying while layer 16k runs.  A layer fed by an earlier layer keeps its own
+prep kernel.  Either way the outputs must equal the single calls' bit
 for bit (the copy is the same bytes, made earlier).
 """
 import pytest
@@ -116,13 +117,17 @@ def test_layers_fed_by_earlier_layers_keep_their_prep(cuda_device):
     dl.graph_cache_clear()
 
 
-def test_only_the_first_16_layers_are_copied_ahead(cuda_device):
-    """70 small FP8 layers with their own x: layers 0..15 copied ahead (layer 0's
-    copy, then 15 in one launch), layers 16..69 each with its own prep."""
+def test_copies_made_ahead_in_windows_of_16(cuda_device):
+    """70 small FP8 layers with their own x: layer 0's copy alone before it, then
+    the copies of layers 16k+1 .. 16k+16 in one launch right after layer 16k
+    (five launches), no per-layer prep; with a workspace that holds no copy
+    region every layer has its own prep."""
     specs = [(F8, 128 * (1 + i % 3), 128 * (1 + i % 4), i % 2 == 0) for i in range(70)]
     layers = independent_layers(cuda_device, specs, 2, 97)
     ws = dl.Workspace.for_stream(layers)
-    assert dl.decode_stream_launches(layers, ws) == 2 + 70 + 54
+    assert dl.decode_stream_launches(layers, ws) == 1 + 5 + 70
+    small = dl.Workspace.for_shapes([L.shape() for L in layers], cuda_device)
+    assert dl.decode_stream_launches(layers, small) == 70 + 70
     want = singles(layers, ws)
     st = torch.cuda.Stream()
     got = run(layers, ws, True, st)

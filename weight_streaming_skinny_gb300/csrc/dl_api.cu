@@ -66,8 +66,9 @@ constexpr long long kFirstWaveNum = 7, kFirstWaveDen = 8;
 constexpr long long kStaticSplitMaxUnitsPerCta = 128;
 constexpr long long kMinSegUnits = 8;
 constexpr bool kAlignSegments = true;
-// Layers of a stream whose FP8 activation copies may be made ahead (a bounded
-// amount of up-front work and workspace).
+// FP8 activation copies made ahead inside a stream go in batches: one launch
+// right after every kHoistWindow-th layer (it copies while that layer runs)
+// makes the copies of the hoisted layers among the next kHoistWindow.
 constexpr int kHoistWindow = 16;
 // Stages whose weights a single FP8 call's main kernel fetches while the prep
 // kernel runs (more delays its first activation copy).
@@ -598,12 +599,12 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 // The workspace the layers need one at a time (the largest single plan), and
-// where the FP8 layers among the first kHoistWindow whose activations are
-// ready when the stream starts -- no earlier layer of the stream writes any
-// byte of their x -- keep their f16 copies: one region each after that, so
-// that the copies are made ahead and those layers then follow one another
-// like bf16 layers.  `limit` = the caller's workspace (0: no limit); layers
-// that do not fit get their own prep launch as usual.  off[i] = 0: not
+// where the FP8 layers whose activations are ready when the stream starts --
+// no earlier layer of the stream writes any byte of their x -- keep their f16
+// copies: one region each after that, so that the copies are made ahead (in
+// batches placed every kHoistWindow layers) and those layers then follow one
+// another like bf16 layers.  `limit` = the caller's workspace (0: no limit);
+// layers that do not fit get their own prep launch as usual.  off[i] = 0: not
 // hoisted.
 // Then the FP8 layers fed by the layer just before them -- x is exactly that
 // layer's whole y, a plain linear (act 0) with the same M and staged token
@@ -623,7 +624,7 @@ dl_status plan_stream(const dl_layer* layers, int n, const DeviceInfo& di, size_
     }
     off.assign((size_t)n, 0);
     end = align_up(base, 256);
-    for (int i = 0; i < n && i < kHoistWindow; ++i) {
+    for (int i = 0; i < n; ++i) {
         const dl_layer& L = layers[i];
         if (L.dtype != DL_FP8_B128) continue;
         bool ready = true;
@@ -885,11 +886,15 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
             }
             return DL_OK;
         };
-        // If layer 0 has no copy of its own made here, its kernel may let the
-        // next one start before the kernels before the stream are done: the
-        // copies then all go before it, waiting first.
+        // Layer 0's copy goes alone before it; the copies of the hoisted
+        // layers in (16k, 16k + 16] go in a batch right after layer 16k, which
+        // copies while that layer runs.  If layer 0 has no copy of its own
+        // made here, its kernel may let the next one start before the kernels
+        // before the stream are done: the first window's copies then go
+        // before it, waiting first.
         const bool split = hoist[0] != 0;
-        dl_status r0 = enqueue_copies(0, split ? 1 : n_layers, false);
+        dl_status r0 = enqueue_copies(0, split ? 1 : (n_layers < kHoistWindow + 1 ? n_layers : kHoistWindow + 1),
+                                      false);
         if (r0 != DL_OK) return r0;
         for (int i = 0; i < n_layers; ++i) {
             const dl_layer& L = layers[i];
@@ -929,7 +934,10 @@ dl_status dl_decode_stream(const dl_layer* layers, int n_layers, void* workspace
                 std::string m = g_err;
                 return fail(r, "layer %d: %s", i, m.c_str());
             }
-            if (i == 0 && split && (r = enqueue_copies(1, n_layers, true)) != DL_OK) return r;
+            if (i % kHoistWindow == 0 && (i > 0 || split)) {
+                const int to = i + kHoistWindow + 1 < n_layers ? i + kHoistWindow + 1 : n_layers;
+                if ((r = enqueue_copies(i + 1, to, true)) != DL_OK) return r;
+            }
         }
         return DL_OK;
     };
@@ -1010,18 +1018,27 @@ int dl_decode_stream_launches(const dl_layer* layers, int n_layers, size_t ws_by
     size_t base = 0, end = 0, wslot = 0;
     std::vector<size_t> hoist, fed;
     if (plan_stream(layers, n_layers, di, ws_bytes, base, hoist, end, fed, wslot) != DL_OK) return -1;
-    int later = 0, fp8 = 0, by_epilogue = 0;
+    int hoisted = 0, fp8 = 0, by_epilogue = 0, batches = 0;
     for (int i = 0; i < n_layers; ++i) {
         fp8 += layers[i].dtype == DL_FP8_B128;
-        later += i > 0 && hoist[(size_t)i] != 0;
+        hoisted += hoist[(size_t)i] != 0;
         by_epilogue += fed[(size_t)i] != 0;
     }
-    const int first = hoist[0] != 0;
-    // layer 0's copy, the other copies (kMaxPrepLayers per launch), one main
-    // kernel per layer, and a prep kernel before every other FP8 layer whose
-    // copy the layer before does not make
-    return first + (later + dl::kMaxPrepLayers - 1) / dl::kMaxPrepLayers + n_layers +
-           (fp8 - first - later - by_epilogue);
+    // the batches of copies made ahead, window by window as enqueued: the
+    // first window before layer 0 when layer 0 has no copy of its own, else
+    // layer 0's alone before it and each window after its first layer
+    const bool split = hoist[0] != 0;
+    auto count = [&](int from, int to) {
+        int c = 0;
+        for (int i = from; i < to; ++i) c += hoist[(size_t)i] != 0;
+        return (c + dl::kMaxPrepLayers - 1) / dl::kMaxPrepLayers;
+    };
+    batches += count(0, split ? 1 : (n_layers < kHoistWindow + 1 ? n_layers : kHoistWindow + 1));
+    for (int i = 0; i < n_layers; i += kHoistWindow)
+        if (i > 0 || split) batches += count(i + 1, i + kHoistWindow + 1 < n_layers ? i + kHoistWindow + 1 : n_layers);
+    // one main kernel per layer, and a prep kernel before every other FP8
+    // layer whose copy the layer before does not make
+    return batches + n_layers + (fp8 - hoisted - by_epilogue);
 }
 
 void dl_graph_cache_clear(void) {
