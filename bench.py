@@ -154,8 +154,10 @@ MLP_TOKENS = (1, 2, 4, 6, 8, 16)
 # at M = 1..16 tokens, each dtype.
 # qwen72b_decoder_fp8_m1 / qwen72b_lm_head_bf16_m1: one decoder layer and the
 # lm_head of the whole-model stream on their own (small cases of its launches).
+# gemv_bf16_1024_m1: the 1024 x 1024 bf16 GEMV with bias alone (a latency
+# case whose 2.1 MB stay in L2; its own workload so that profilers can take it).
 WORKLOADS = ["qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6", "qwen72b_model_fp8_m1",
-             "qwen72b_decoder_fp8_m1", "qwen72b_lm_head_bf16_m1"] + [
+             "qwen72b_decoder_fp8_m1", "qwen72b_lm_head_bf16_m1", "gemv_bf16_1024_m1"] + [
     f"qwen72b_mlp_{dt}_m{m}" for dt in ("bf16", "fp8") for m in MLP_TOKENS]
 
 
@@ -182,6 +184,8 @@ def layer_specs(workload: str):
     if workload == "qwen72b_lm_head_bf16_m1":
         N, K, b = inputs.QWEN72B_LM_HEAD
         return [(inputs.DTYPE_BF16, 1, N, K, b, "lm_head", 2)], 4
+    if workload == "gemv_bf16_1024_m1":
+        return [(inputs.DTYPE_BF16, 1, 1024, 1024, True, "gemv", 0)], 0
     if workload.startswith("qwen72b_mlp_"):
         _, _, dt, m = workload.split("_")
         dtype = inputs.DTYPE_BF16 if dt == "bf16" else inputs.DTYPE_FP8_B128
@@ -297,10 +301,10 @@ def time_steps(torch, step, stream, steps, per_step=True):
 def single_call_times(torch, dl, calls, stream, reps):
     """Isolated call times: an event pair around every call (events break the
     overlap with the neighbouring launches), calls cycled through `calls`
-    (distinct weights keep L2 cold).  A short spin kernel before each pair
-    keeps the GPU busy while the host enqueues the call, so that the pair
-    measures the call on the device, not the host's submission.  Returns
-    per-call ms."""
+    (distinct weights, together at least 3 x L2, keep L2 cold).  A short spin
+    kernel before each pair keeps the GPU busy while the host enqueues the
+    call, so that the pair measures the call on the device, not the host's
+    submission.  Returns per-call ms."""
     n = len(calls)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
@@ -332,11 +336,21 @@ def stream_rate(torch, dl, layers, ys, stream, steps, warmup):
     return total / steps, each, nbytes
 
 
+def cold_copies(L, l2_bytes) -> int:
+    """Distinct copies of a layer that single calls rotate over so that each
+    call finds none of its bytes in L2: ceil(3 x L2 / the layer's bytes)."""
+    return max(1, -(-3 * l2_bytes // L.algorithmic_bytes))
+
+
 def layer_config_summary(torch, dl, workload, dev, stream, peak, steps=60, warmup=5):
     """An untimed-by-the-contract summary of one of the layer workloads: the
     4-layer stream (graph replay), each layer's in-stream cost as the
     difference between the full stream and the stream without it, and each
-    layer's isolated single-call time."""
+    layer's isolated single-call time (calls rotated over distinct copies of
+    the layer: some of these layers are smaller than L2)."""
+    from weight_streaming_skinny_gb300 import inputs
+    _, cfg = layer_specs(workload)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     layers = build_layers(workload, dev)
     ys = [out_buffer(L, dev) for _, L in layers]
     ms, each, nbytes = stream_rate(torch, dl, layers, ys, stream, steps, warmup)
@@ -351,13 +365,21 @@ def layer_config_summary(torch, dl, workload, dev, stream, peak, steps=60, warmu
                                     stream, steps, warmup)
         d = ms - ms_rest
         b = out_bytes(L)
-        call = single_call_times(torch, dl, [layer_call(dl, L, ys[j], ws, stream)], stream, 30)[5:]
+        calls = [layer_call(dl, L, ys[j], ws, stream)]
+        for c in range(1, cold_copies(L, l2)):
+            Lc = inputs.make_layer(L.dtype, L.M, L.N, L.K, bias=L.bias is not None, config_id=cfg,
+                                   layer_idx=1000 + 10 * j + c, device=dev)
+            Lc.act = L.act
+            calls.append(layer_call(dl, Lc, out_buffer(Lc, dev), ws, stream))
+        call = single_call_times(torch, dl, calls, stream, 30)[5:]
+        n_copies = len(calls)
+        del calls
         med = statistics.median(call)
         out["layers"][name] = {
             "bytes": b,
             "in_stream_us": round(d * 1e3, 3),
             "in_stream_frac": round(b / (d * 1e-3) / 1e9 / peak, 4) if d > 0 else None,
-            "single_call": _dist_us(call),
+            "single_call": {**_dist_us(call), "copies": n_copies},
             "single_call_frac": round(b / (med * 1e-3) / 1e9 / peak, 4)}
     out["in_stream_method"] = ("in_stream_us = step time of the 4-layer stream minus that of the "
                                "stream without the layer (graph replay, 60 steps each)")
@@ -607,22 +629,51 @@ def run_ours(args, rank, world, dist):
     if is_model:
         res["ms_per_token"] = round(ms_per_step, 4)
 
+    # ---- the whole token without graph capture: the same layer list enqueued
+    # launch by launch from the host on every step (programmatic dependent
+    # launch kept), after the timed region
+    if is_model and not args.skip_extras and use_graph:
+        ng_step = lambda: dl.decode_stream(dl_layers, ws, use_graph=False, stream=stream)  # noqa: E731
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                ng_step()
+        stream.synchronize()
+        ng_ms, ng_each = time_steps(torch, ng_step, stream, 20)
+        res["no_graph"] = {"ms_per_token": round(ng_ms / 20, 4), "step": _dist_us(ng_each),
+                           "GB/s": round(step_bytes / (ng_ms / 20 * 1e-3) / 1e9, 1),
+                           "note": "dl_decode_stream without graph capture: every step enqueues "
+                                   "its launches from the host"}
+
     # ---- the other single-GPU configurations, after the timed region
     if is_model and not args.skip_extras:
         del dl_layers, ws
         extra = {}
         for wl in ("qwen72b_layer_bf16_m1", "qwen72b_layer_fp8_m6"):
             extra[wl] = layer_config_summary(torch, dl, wl, dev, stream, peak)
-        # the 1024 x 1024 bf16 GEMV with bias: a latency configuration (its
-        # 2 MB stay in L2), microseconds per isolated call
+        # the 1024 x 1024 bf16 GEMV with bias, a latency configuration:
+        # microseconds per isolated call, warm (its 2.1 MB stay in L2 from one
+        # call to the next) and cold (calls rotated over ceil(3 L2 / 2.1 MB)
+        # distinct copies of the layer, so that each call's bytes were evicted)
         L0 = inputs.make_layer(inputs.DTYPE_BF16, 1, 1024, 1024, bias=True, config_id=0, device=dev)
         L0.act = 0
         y0 = out_buffer(L0, dev)
         ws0 = dl.Workspace(dl.workspace_bytes(1, 1024, 1024, dl.BF16), dev)
         t = single_call_times(torch, dl, [layer_call(dl, L0, y0, ws0, stream)], stream, 220)[20:]
+        n_cold = cold_copies(L0, torch.cuda.get_device_properties(dev).L2_cache_size)
+        cold = []
+        for i in range(n_cold):
+            Li = inputs.make_layer(inputs.DTYPE_BF16, 1, 1024, 1024, bias=True, config_id=0,
+                                   layer_idx=i + 1, device=dev)
+            Li.act = 0
+            cold.append(layer_call(dl, Li, out_buffer(Li, dev), ws0, stream))
+        tc = single_call_times(torch, dl, cold, stream, 2 * n_cold + 20)[20:]
         extra["gemv_bf16_1024_m1"] = {**_dist_us(t), "bytes": L0.algorithmic_bytes,
                                       "note": "latency configuration: 2.1 MB, L2-resident after "
-                                              "the first call"}
+                                              "the first call",
+                                      "cold_l2": {**_dist_us(tc), "copies": n_cold,
+                                                  "note": "calls rotated over distinct copies "
+                                                          "(3 x L2 bytes in all)"}}
+        del cold
         res["configs"] = extra
     return res, layers
 
@@ -719,8 +770,11 @@ def main():
     config = {"workload": args.workload,
               "layers": [{"name": s[5], "dtype": s[0], "M": s[1], "N": s[2], "K": s[3],
                           "bias": s[4]} for s in specs],
-              "l2": "inputs larger than L2: every step streams every weight matrix of the "
-                    "workload (each step >= 0.7 GB) through a 129 MB L2",
+              "l2": ("L2-resident: a latency case, its 2.1 MB are L2 hits after the first "
+                     "step (cold-L2 calls: the model line's configs.gemv_bf16_1024_m1.cold_l2)"
+                     if args.workload == "gemv_bf16_1024_m1" else
+                     "inputs larger than L2: every step streams every weight matrix of the "
+                     "workload (each step >= 0.7 GB) through a 129 MB L2"),
               "parallelism": f"replicas x{world}", "kernel_family": args.kernel,
               "mode": args.mode}
     if len(specs) > 8:
@@ -811,8 +865,9 @@ def main():
         if is_model:
             line["ms_per_token"] = res["ms_per_token"]
             line["ceiling_ratio"] = round(res["ceiling_ms_at_measured_peak"] / res["ms_per_token"], 4)
-        if "configs" in res:
-            line["configs"] = res["configs"]
+        for k in ("no_graph", "configs"):
+            if k in res:
+                line[k] = res[k]
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

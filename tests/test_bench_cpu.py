@@ -89,3 +89,13 @@ def test_percentiles():
     assert bench._pctl(vals, 0.1) == 1.0 and bench._pctl(vals, 0.9) == 9.0
     d = bench._dist_us([0.001, 0.002, 0.003])
     assert d["median_us"] == 2.0 and d["n"] == 3
+
+
+def test_cold_copies_cover_three_l2():
+    l2 = 129 * 10**6
+    for dt, N, K, bias, want in (("bf16", 10240, 8192, True, 3), ("fp8_b128", 8192, 8192, False, 6),
+                                 ("bf16", 59136, 8192, False, 1), ("bf16", 1024, 1024, True, 184)):
+        L = inputs.LayerInputs(dt, 1, N, K, None, None, None, object() if bias else None)
+        n = bench.cold_copies(L, l2)
+        assert n == want and n * L.algorithmic_bytes >= 3 * l2
+        assert n == 1 or (n - 1) * L.algorithmic_bytes < 3 * l2
