@@ -121,7 +121,10 @@ dl_status dl_linear_bf16(const void* x, const void* W, const void* bias, void* y
 /*
  * y = x . dequant(Wq)^T (+ bias), weight-only FP8 with 128x128 block scales.
  *   Wq     e4m3 (E4M3FN) codes [N][K] as bytes, 16-byte aligned, K % 128 == 0
- *   scales fp32 [ceil(N/128)][K/128] row-major: scales[n/128][k/128]
+ *   scales fp32 [ceil(N/128)][K/128] row-major: scales[n/128][k/128], 4-byte
+ *          aligned; the kernel copies them in 16-byte-aligned pieces, so it
+ *          may also read up to 12 bytes just before scales[0] (the rest of
+ *          that 16-byte block, always in the same page), never after the end
  *   other arguments as for dl_linear_bf16.
  * Each e4m3 code is decoded exactly (NaN codes 0x7F/0xFF decode to NaN); the
  * block scale multiplies the fp32 partial sum of each 128-wide K block, which

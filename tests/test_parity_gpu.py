@@ -171,6 +171,30 @@ def test_power_of_two_scales_scale_outputs_exactly(cuda_device, family):
 
 
 @pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("off", [1, 2, 3])
+def test_fp8_scales_not_16_byte_aligned(cuda_device, family, off):
+    """Block scales 4, 8 or 12 bytes past a 16-byte boundary, with an odd
+    number of K blocks (K = 640: a stage's two scales may straddle a 16-byte
+    block, the last unit of a tile has one) and a ragged last tile.  The
+    floats around the scales are NaN, so reading a neighbour as a scale would
+    show.  Same outputs, bit for bit, as with the scales at an aligned
+    address, and within the oracle's bound."""
+    dl.set_override(family, 0, 0)
+    L = inputs.make_layer(inputs.DTYPE_FP8_B128, 6, 300, 640, bias=True, config_id=42).to(cuda_device)
+    y_al, y32_al = run_gpu(L, cuda_device)
+    n = L.scales.numel()
+    buf = torch.full((n + 8,), float("nan"), dtype=torch.float32, device=cuda_device)
+    view = buf[off:off + n].view(L.scales.shape)
+    view.copy_(L.scales)
+    assert view.data_ptr() % 16 == 4 * off
+    Lo = inputs.LayerInputs(L.dtype, L.M, L.N, L.K, L.x, L.w, view, L.bias)
+    y, y32 = run_gpu(Lo, cuda_device)
+    assert torch.equal(y32, y32_al) and torch.equal(y, y_al)
+    ref, a = oracle_for(L)
+    assert_parity(y, y32, ref, a, what=f"fp8 scales at +{4 * off} B fam={family}")
+
+
+@pytest.mark.parametrize("family", FAMILIES)
 def test_row_permutation_within_tiles_permutes_outputs_bitwise(cuda_device, family):
     dl.set_override(family, 0, 0)
     for dtype in (inputs.DTYPE_BF16, inputs.DTYPE_FP8_B128):

@@ -353,7 +353,8 @@ dl_status get_encode(EncodeTiledFn& fn) {
 }
 
 dl_status encode_maps(const Plan& pl, int M, int N, int K, const void* x, const void* W,
-                      CUtensorMap& tw, CUtensorMap& tx) {
+                      const float* scales, CUtensorMap& tw, CUtensorMap& tx, CUtensorMap& ts,
+                      int& scale_off) {
     EncodeTiledFn enc;
     dl_status s = get_encode(enc);
     if (s != DL_OK) return s;
@@ -402,6 +403,26 @@ dl_status encode_maps(const Plan& pl, int M, int N, int K, const void* x, const 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) return fail(DL_ERR_CUDA, "activation tensor map: CUresult %d", (int)r);
+    scale_off = 0;
+    if (pl.dtype == DL_BF16) {
+        ts = tx;                               // not read by the bf16 kernels
+        return DL_OK;
+    }
+    // The block scales as one row of fp32, from the scales rounded down to 16
+    // bytes (the tensor map's base must be; scales need only 4) so that
+    // scales[i] is element scale_off + i.  The 16-byte block around scales[0]
+    // lies in the same page, allocations begin on 256-byte boundaries, and
+    // boxes that run past the last scale read zeros.
+    const uintptr_t a = reinterpret_cast<uintptr_t>(scales);
+    const uintptr_t base = a & ~static_cast<uintptr_t>(15);
+    scale_off = static_cast<int>((a - base) / sizeof(float));
+    const cuuint64_t sdims[1] = {(cuuint64_t)scale_off + (cuuint64_t)pl.n_tiles * pl.KB};
+    const cuuint64_t sstrides[1] = {0};        // (rank 1: no strides are read)
+    const cuuint32_t sbox[1] = {8};
+    r = enc(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, reinterpret_cast<void*>(base), sdims, sstrides,
+            sbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DL_ERR_CUDA, "block-scale tensor map: CUresult %d", (int)r);
     return DL_OK;
 }
 
@@ -459,14 +480,17 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
         xh = xh_ready;
         unscale = unscale_ready;
     }
-    CUtensorMap tw, tx;
-    if ((s = encode_maps(pl, M, N, K, xh ? static_cast<const void*>(xh) : x, W, tw, tx)) != DL_OK)
+    CUtensorMap tw, tx, ts;
+    int scale_off = 0;
+    if ((s = encode_maps(pl, M, N, K, xh ? static_cast<const void*>(xh) : x, W, scales, tw, tx, ts,
+                         scale_off)) != DL_OK)
         return s;
     dl::LinearParams p;
     p.bias = static_cast<const uint16_t*>(bias);
     p.y = static_cast<uint16_t*>(y);
     p.y_f32 = y_f32;
     p.scales = scales;
+    p.scale_off = scale_off;
     p.x = static_cast<const uint16_t*>(x);
     p.unscale = unscale;
     p.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.counter_off);
@@ -516,7 +540,7 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
         // during the short prep; inside a stream it lets main launch at once,
         // so main fills its whole ring during the previous layer's tail.
         p.early_stages = after_own ? pl.stages : kEarlyStagesAfterPrep;
-        e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, false);
+        e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, ts, p, pl.grid, pl.smem, stream, false);
         if (e == cudaSuccess && !prepped) {
             dl::PrepBatch b{};
             b.n = 1;
@@ -525,7 +549,7 @@ dl_status launch_layer(int dtype, int M, int N, int K, const void* x, const void
             e = dl::launch_prep_x(b, after_own, stream);
         }
         if (e == cudaSuccess)
-            e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, stream, true);
+            e = dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, ts, p, pl.grid, pl.smem, stream, true);
     }
     if (e != cudaSuccess) return fail(DL_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return DL_OK;
@@ -538,11 +562,11 @@ dl_status prepare_layer(int dtype, int M, int N, int K, const DeviceInfo& di) {
     Plan pl;
     dl_status s = make_plan(dtype, M, N, K, di, pl);
     if (s != DL_OK) return s;
-    CUtensorMap tw, tx;
+    CUtensorMap tw, tx, ts;
     dl::LinearParams p;
     cudaError_t e = dtype == DL_BF16
         ? dl::launch_linear_bf16(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, nullptr, false)
-        : dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, p, pl.grid, pl.smem, nullptr, false);
+        : dl::launch_linear_fp8(pl.family, pl.mt, tw, tx, ts, p, pl.grid, pl.smem, nullptr, false);
     if (e != cudaSuccess) return fail(DL_ERR_CUDA, "kernel attribute: %s", cudaGetErrorString(e));
     return DL_OK;
 }

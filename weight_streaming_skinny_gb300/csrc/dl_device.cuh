@@ -130,6 +130,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// One box of a one-dimensional tensor map at element c0 (c0 * element size a
+// multiple of 16 bytes); elements past the tensor's end arrive as zeros.
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0) {
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0)
+        : "memory");
+}
+
 // Bulk (non-tensor) copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) global -> this CTA's shared memory, counted as transaction bytes
 // on the barrier.
@@ -139,22 +149,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
-}
-
-// Asynchronous global -> shared copies (4 or 16 bytes, both addresses aligned
-// to the size) and the barrier arrival that tracks them: the barrier's pending
-// count is raised at once and lowered when every earlier cp.async of this
-// thread has landed, so the phase cannot complete before they do.
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ---------------------------------------------------------------- shared loads

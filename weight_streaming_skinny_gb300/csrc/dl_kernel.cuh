@@ -138,6 +138,8 @@ struct LinearParams {
     uint16_t* y;              // bf16 [M][N]
     float* y_f32;             // fp32 [M][N] or null
     const float* scales;      // fp32 [ceil(N/128)][KB] (FP8)
+    int scale_off;            // FP8: elements between the scales tensor map's base (the
+                              //   scales rounded down to 16 bytes) and scales[0] (0..3)
     const uint16_t* x;        // bf16 [M][K] (FP8: read only by units not exact in f16)
     const float* unscale;     // fp32 [KB][16] (FP8): 2^-s of the f16 copy, 0 = not exact
     int* counter;             // [0]: segments claimed after the first wave, [1]: CTAs done
@@ -183,16 +185,21 @@ struct LinearParams {
 constexpr int kMaxUnitsPerStage = 2;
 
 struct StageHeader {
+    // FP8: one tensor copy of 8 block scales (32 bytes; a tensor copy lands
+    // on a 128-byte boundary, so the header is 256 bytes and the box comes
+    // first): the scale of K block kb is scale8[soff], of kb + 1 scale8[soff + 1]
+    float scale8[8];
     int tile;                 // units held by the stage: weight rows 128*tile..,
     int kb;                   //   K blocks kb .. kb + nkb - 1
     int seg;                  // segment they belong to
     int flags;                // kRunFirst | kRunLast | kDone
     int nkb;                  // units in the stage (1, or 2 for FP8)
-    float scale[kMaxUnitsPerStage];  // FP8 block scales (copied asynchronously)
-    int pad;
+    int soff;                 // FP8: position of K block kb's scale in scale8 (0..3)
+    int pad[2];
     float unscale[kMaxUnitsPerStage][kUnscaleStride];   // FP8: per-token unscale factors
+    int pad2[16];
 };
-static_assert(sizeof(StageHeader) == 160, "stage header layout");
+static_assert(sizeof(StageHeader) == 256, "stage header layout");
 
 template <int DT>
 struct TileBytes {
@@ -1153,7 +1160,7 @@ __device__ __forceinline__ void fixup_tile_swiglu(const LinearParams& p, int til
 template <int DT, int FAM, int MT>
 __global__ void __launch_bounds__(threads_for(DT, FAM), min_blocks_for(DT, FAM, MT))
 linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-              const LinearParams p) {
+              const __grid_constant__ CUtensorMap tm_s, const LinearParams p) {
     using Consumer = typename ConsumerOf<DT, FAM, MT>::type;
     constexpr int MTB = XRows<MT>::v;
     constexpr int W_UNIT = TileBytes<DT>::w;                 // weights of one unit
@@ -1213,6 +1220,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (warp == kLoaderWarp && lane == 0) {
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_x);
+        if constexpr (DT == kFP8) prefetch_tmap(&tm_s);
     }
     if constexpr (FAM == kTC) {
         // The accumulators of two stages (two units each) in tensor memory.
@@ -1330,6 +1338,11 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 } else {
                     for (int u = 0; u < nkb; ++u)
                         tma_load_2d(dw + u * W_UNIT, &tm_w, bar, (kb + u) * kBK, tile * kBN, pol_w);
+                    // The block scales of K blocks kb, kb + 1 (elements e, e + 1
+                    // of the scales map): one box of 8 from e rounded down to a
+                    // multiple of 4 (16 bytes) holds both.
+                    const int e = p.scale_off + tile * KB + kb;
+                    tma_load_1d(smem_u32(&hdr[s].scale8[0]), &tm_s, bar, e & ~3);
                 }
             };
             // Activations of the stage.  bf16: x itself (two 64-column boxes).
@@ -1367,10 +1380,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 const uint32_t bar = smem_u32(&full[s]);
                 uint32_t bytes = 0;
                 if constexpr (DT == kFP8) {
-                    for (int u = 0; u < nkb; ++u)
-                        cp_async_4(smem_u32(&hdr[s].scale[u]), p.scales + (long long)tile * KB + kb + u);
-                    cp_async_mbar_arrive(bar);
-                    bytes = nkb * (W_UNIT + kUnscaleStride * 4) + X_STAGE;
+                    hdr[s].soff = (p.scale_off + tile * KB + kb) & 3;   // see issue_w
+                    bytes = nkb * (W_UNIT + kUnscaleStride * 4) + X_STAGE + 8 * 4;
                 } else {
                     bytes = W_UNIT + X_UNIT;
                 }
@@ -1562,7 +1573,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             if (warp < 4) {
 #pragma unroll
                 for (int uu = 0; uu < 2; ++uu) {
-                    sc[uu] = hd.scale[uu];
+                    sc[uu] = hd.scale8[hd.soff + uu];
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         u[uu][m] = hd.unscale[uu][m];
@@ -1594,9 +1605,10 @@ linear_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         } else {
             if constexpr (DT == kFP8) {
                 nkb = hd.nkb;
-                c.consume(sw, sx, hd.scale[0], hd.unscale[0], kb, p, warp, lane);
+                const int so = hd.soff;
+                c.consume(sw, sx, hd.scale8[so], hd.unscale[0], kb, p, warp, lane);
                 if (nkb == 2)
-                    c.consume(sw + W_UNIT, sx + X_UNIT, hd.scale[1], hd.unscale[1], kb + 1, p, warp, lane);
+                    c.consume(sw + W_UNIT, sx + X_UNIT, hd.scale8[so + 1], hd.unscale[1], kb + 1, p, warp, lane);
             } else {
                 c.consume(sw, sx, 1.f, nullptr, kb, p, warp, lane);
             }

@@ -6,7 +6,8 @@ namespace dl {
 cudaError_t launch_linear_bf16(int family, int mt, const CUtensorMap& tw, const CUtensorMap& tx,
                                const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
                                bool launch) {
-    return launch_family<kBF16>(family, mt, tw, tx, p, grid, smem, stream, launch);
+    // (bf16 has no block scales: the kernel never reads its third map)
+    return launch_family<kBF16>(family, mt, tw, tx, tx, p, grid, smem, stream, launch);
 }
 
 int host_smem_bytes(int dtype, int family, int mt, int stages) {

@@ -25,7 +25,8 @@ cudaError_t prepare_instance(size_t smem) {
 }
 
 template <int DT, int FAM, int MT>
-cudaError_t launch_instance(const CUtensorMap& tw, const CUtensorMap& tx, const LinearParams& p,
+cudaError_t launch_instance(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
+                            const LinearParams& p,
                             int grid, size_t smem, cudaStream_t stream, bool launch) {
     cudaError_t e = prepare_instance<DT, FAM, MT>(smem);
     if (e != cudaSuccess || !launch) return e;
@@ -42,38 +43,39 @@ cudaError_t launch_instance(const CUtensorMap& tw, const CUtensorMap& tx, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, linear_kernel<DT, FAM, MT>, tw, tx, p);
+    e = cudaLaunchKernelEx(&cfg, linear_kernel<DT, FAM, MT>, tw, tx, ts, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int DT>
 cudaError_t launch_family(int family, int mt, const CUtensorMap& tw, const CUtensorMap& tx,
+                          const CUtensorMap& ts,
                           const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
                           bool launch) {
     if (family == kMMA) {
-        if (mt == 8) return launch_instance<DT, kMMA, 8>(tw, tx, p, grid, smem, stream, launch);
-        if (mt == 16) return launch_instance<DT, kMMA, 16>(tw, tx, p, grid, smem, stream, launch);
+        if (mt == 8) return launch_instance<DT, kMMA, 8>(tw, tx, ts, p, grid, smem, stream, launch);
+        if (mt == 16) return launch_instance<DT, kMMA, 16>(tw, tx, ts, p, grid, smem, stream, launch);
         return cudaErrorInvalidValue;
     }
     if (family == kTC) {
         // tensor-memory family: FP8 weights only (kind::f8f6f4 MMAs)
         if constexpr (DT == kFP8) {
-            if (mt == 8) return launch_instance<DT, kTC, 8>(tw, tx, p, grid, smem, stream, launch);
-            if (mt == 16) return launch_instance<DT, kTC, 16>(tw, tx, p, grid, smem, stream, launch);
+            if (mt == 8) return launch_instance<DT, kTC, 8>(tw, tx, ts, p, grid, smem, stream, launch);
+            if (mt == 16) return launch_instance<DT, kTC, 16>(tw, tx, ts, p, grid, smem, stream, launch);
         }
         return cudaErrorInvalidValue;
     }
     switch (mt) {
-        case 1: return launch_instance<DT, kSIMT, 1>(tw, tx, p, grid, smem, stream, launch);
-        case 2: return launch_instance<DT, kSIMT, 2>(tw, tx, p, grid, smem, stream, launch);
+        case 1: return launch_instance<DT, kSIMT, 1>(tw, tx, ts, p, grid, smem, stream, launch);
+        case 2: return launch_instance<DT, kSIMT, 2>(tw, tx, ts, p, grid, smem, stream, launch);
         default: break;
     }
     if constexpr (DT == kBF16) {
         // FP8 SIMT stops at 2 tokens (the host plan switches to MMA beyond).
-        if (mt == 4) return launch_instance<DT, kSIMT, 4>(tw, tx, p, grid, smem, stream, launch);
-        if (mt == 8) return launch_instance<DT, kSIMT, 8>(tw, tx, p, grid, smem, stream, launch);
-        if (mt == 16) return launch_instance<DT, kSIMT, 16>(tw, tx, p, grid, smem, stream, launch);
+        if (mt == 4) return launch_instance<DT, kSIMT, 4>(tw, tx, ts, p, grid, smem, stream, launch);
+        if (mt == 8) return launch_instance<DT, kSIMT, 8>(tw, tx, ts, p, grid, smem, stream, launch);
+        if (mt == 16) return launch_instance<DT, kSIMT, 16>(tw, tx, ts, p, grid, smem, stream, launch);
     }
     return cudaErrorInvalidValue;
 }

@@ -94,9 +94,9 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const __grid_constant__ Pre
 }
 
 cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const CUtensorMap& tx,
-                              const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
-                              bool launch) {
-    return launch_family<kFP8>(family, mt, tw, tx, p, grid, smem, stream, launch);
+                              const CUtensorMap& ts, const LinearParams& p, int grid, size_t smem,
+                              cudaStream_t stream, bool launch) {
+    return launch_family<kFP8>(family, mt, tw, tx, ts, p, grid, smem, stream, launch);
 }
 
 // One layer per launch passes a small parameter block (NB = 1); batches up to

@@ -20,13 +20,15 @@ int host_min_blocks(int dtype, int family, int mt);
 
 // Launch the (dtype, family, mt) instance (launch = false: only raise its
 // shared-memory ceiling on the current device, which is done once per device
-// and never during stream capture).  Returns the first CUDA error.
+// and never during stream capture).  Returns the first CUDA error.  tw: the
+// weights, tx: the activations (FP8: their f16 copy or e4m3 parts), ts (FP8):
+// the block scales as a one-dimensional fp32 map (boxes of 8).
 cudaError_t launch_linear_bf16(int family, int mt, const CUtensorMap& tw, const CUtensorMap& tx,
                                const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
                                bool launch);
 cudaError_t launch_linear_fp8(int family, int mt, const CUtensorMap& tw, const CUtensorMap& tx,
-                              const LinearParams& p, int grid, size_t smem, cudaStream_t stream,
-                              bool launch);
+                              const CUtensorMap& ts, const LinearParams& p, int grid, size_t smem,
+                              cudaStream_t stream, bool launch);
 
 // FP8 activation prep of up to kMaxPrepLayers layers in one launch: for each,
 // x (bf16 [M][K]) -> xh (f16 [KB][2][mtb][64], exact per-block power-of-two
