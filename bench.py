@@ -342,14 +342,18 @@ def cold_copies(L, l2_bytes) -> int:
     return max(1, -(-3 * l2_bytes // L.algorithmic_bytes))
 
 
-def layer_config_summary(torch, dl, workload, dev, stream, peak, steps=60, warmup=5):
+def layer_config_summary(torch, dl, workload, dev, stream, peak, steps=60, warmup=5, repeats=8):
     """An untimed-by-the-contract summary of one of the layer workloads: the
-    4-layer stream (graph replay), each layer's in-stream cost as the
-    difference between the full stream and the stream without it, and each
-    layer's isolated single-call time (calls rotated over distinct copies of
-    the layer: some of these layers are smaller than L2)."""
+    configured step (its 4 layers as one graph replay); each layer's in-stream
+    cost, measured inside a stream of `repeats` copies of the layer set
+    (distinct weights, one graph, as consecutive decoder layers of a decode
+    step run) as (the stream's time - the time of the same stream without
+    every copy of that layer) / repeats, and also the same difference in the
+    4-layer graph alone, where the first layer pays the graph's start; and
+    each layer's isolated single call, rotated over the copies (some of these
+    layers are smaller than L2)."""
     from weight_streaming_skinny_gb300 import inputs
-    _, cfg = layer_specs(workload)
+    specs, cfg = layer_specs(workload)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     layers = build_layers(workload, dev)
     ys = [out_buffer(L, dev) for _, L in layers]
@@ -357,33 +361,47 @@ def layer_config_summary(torch, dl, workload, dev, stream, peak, steps=60, warmu
     out = {"ms_per_step": round(ms, 5), "step": _dist_us(each),
            "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
            "frac_measured": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "layers": {}}
+    # `repeats` copies of the layer set, in decoder order, distinct seeds
+    big, big_ys = [], []
+    for r in range(repeats):
+        for i, (dt, M, N, K, bias, name, act) in enumerate(specs):
+            Lr = inputs.make_layer(dt, M, N, K, bias=bias, config_id=cfg, layer_idx=100 + 4 * r + i,
+                                   device=dev)
+            Lr.act = act
+            big.append((name, Lr))
+            big_ys.append(out_buffer(Lr, dev))
+    ms_big, _, _ = stream_rate(torch, dl, big, big_ys, stream, steps // 2, warmup)
     ws = dl.Workspace.for_shapes([(L.M, L.N, L.K, dl.BF16 if L.dtype == "bf16" else dl.FP8_B128)
                                   for _, L in layers], dev)
     for j, (name, L) in enumerate(layers):
-        rest = [layers[i] for i in range(len(layers)) if i != j]
-        ms_rest, _, _ = stream_rate(torch, dl, rest, [ys[i] for i in range(len(layers)) if i != j],
-                                    stream, steps, warmup)
-        d = ms - ms_rest
         b = out_bytes(L)
-        calls = [layer_call(dl, L, ys[j], ws, stream)]
-        for c in range(1, cold_copies(L, l2)):
-            Lc = inputs.make_layer(L.dtype, L.M, L.N, L.K, bias=L.bias is not None, config_id=cfg,
-                                   layer_idx=1000 + 10 * j + c, device=dev)
-            Lc.act = L.act
-            calls.append(layer_call(dl, Lc, out_buffer(Lc, dev), ws, stream))
+        keep = [q for q in range(len(big)) if big[q][0] != name]
+        ms_rest, _, _ = stream_rate(torch, dl, [big[q] for q in keep], [big_ys[q] for q in keep],
+                                    stream, steps // 2, warmup)
+        d = (ms_big - ms_rest) / repeats
+        rest = [layers[i] for i in range(len(layers)) if i != j]
+        ms_rest4, _, _ = stream_rate(torch, dl, rest, [ys[i] for i in range(len(layers)) if i != j],
+                                     stream, steps, warmup)
+        d4 = ms - ms_rest4
+        # single calls rotate over the copies (at least ceil(3 L2 / bytes) of them)
+        copies = [q for q in range(len(big)) if big[q][0] == name]
+        assert len(copies) >= cold_copies(L, l2)
+        calls = [layer_call(dl, big[q][1], big_ys[q], ws, stream) for q in copies]
         call = single_call_times(torch, dl, calls, stream, 30)[5:]
-        n_copies = len(calls)
-        del calls
         med = statistics.median(call)
         out["layers"][name] = {
             "bytes": b,
             "in_stream_us": round(d * 1e3, 3),
             "in_stream_frac": round(b / (d * 1e-3) / 1e9 / peak, 4) if d > 0 else None,
-            "single_call": {**_dist_us(call), "copies": n_copies},
+            "in_stream_4_layer_graph_us": round(d4 * 1e3, 3),
+            "in_stream_4_layer_graph_frac": round(b / (d4 * 1e-3) / 1e9 / peak, 4) if d4 > 0 else None,
+            "single_call": {**_dist_us(call), "copies": len(calls)},
             "single_call_frac": round(b / (med * 1e-3) / 1e9 / peak, 4)}
-    out["in_stream_method"] = ("in_stream_us = step time of the 4-layer stream minus that of the "
-                               "stream without the layer (graph replay, 60 steps each)")
-    del layers, ys
+    out["in_stream_method"] = (f"in_stream_us = (time of a stream of {repeats} copies of the 4 layers, "
+                               f"distinct weights, one graph - the same stream without every copy of "
+                               f"the layer) / {repeats}; in_stream_4_layer_graph_us = the 4-layer "
+                               f"graph minus the graph without the layer")
+    del layers, ys, big, big_ys
     return out
 
 
